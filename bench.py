@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the batch-1 dequant GEMV on one node.
+
+One step = the Q4_K decode projections of a Llama-8B-like layer (QKV 6144x4096, gate+up
+28672x4096, down 4096x14336): three GEMVs through the C-ABI.  Weights are synthetic and
+seeded, resident in HBM, rotated over enough copies that each step reads from HBM (the
+whole set of copies is > 3x the L2 size).  Timed on the device with CUDA events around
+replays of a CUDA graph holding the steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on the
+host cores, on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from quantized_weight_dequant_gb300 import synth  # noqa: E402
+
+METRIC = "fused dequant-GEMV achieved HBM GB/s and µs/call at M=1 (fraction of GB300 peak)"
+
+# name -> list of (label, fmt, N, K, activation key).  GEMVs sharing an activation key
+# read the same x (the layer's hidden vector or its MLP activation).
+WORKLOADS = {
+    "q4k_llama8b_decode": [("qkv", synth.Q4_K, 6144, 4096, "h"), ("gate_up", synth.Q4_K, 28672, 4096, "h"),
+                           ("down", synth.Q4_K, 4096, 14336, "m")],
+    "q4k_1024x1024": [("w", synth.Q4_K, 1024, 1024, "h")],
+    "nvfp4_4096x14336": [("w", synth.NVFP4, 4096, 14336, "h")],
+    "nvfp4_14336x4096": [("w", synth.NVFP4, 14336, 4096, "h")],
+    "tq1_0_4096x4096": [("w", synth.TQ1_0, 4096, 4096, "h")],
+    "tq1_0_11008x4096": [("w", synth.TQ1_0, 11008, 4096, "h")],
+    "layer_mixed": [(p, synth.LAYER_MIXED[p], n, k, "m" if p == "down" else "h") for p, n, k in synth.LAYER_SHAPES],
+}
+for _p, _n, _k in synth.LAYER_SHAPES:
+    for _f in (synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.Q8_0):
+        WORKLOADS[f"layer_{_p}_{synth.FORMAT_NAMES[_f]}"] = [(_p, _f, _n, _k, "h")]
+DEFAULT_WORKLOAD = "q4k_llama8b_decode"
+
+
+def gemv_bytes(fmt, N, K) -> int:
+    """Algorithmic bytes of one GEMV: packed weights + x (2 B/elem) + y (4 B/elem)."""
+    return synth.packed_bytes(fmt, N, K) + 2 * K + 4 * N
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks sampler
+class Clocks:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int, uuid: str | None):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        target = f"GPU-{uuid}" if uuid else str(device_index)
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}",
+                                          "--format=csv,noheader,nounits", "-lms", "100", "-i", target],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+class OracleSampler:
+    """Times the CPU oracle on row samples of every GEMV of a workload (host cores)."""
+
+    def __init__(self, gemvs, threads: int, seed: int = 0):
+        import oracle
+        self.oracle = oracle
+        self.threads = threads
+        self.pool = cf.ThreadPoolExecutor(max_workers=threads)  # the C oracle releases the GIL
+        self.data = []
+        for label, fmt, N, K, _ in gemvs:
+            self.data.append((label, fmt, N, K, synth.make_weights(fmt, N, K, seed), synth.make_x(fmt, K, seed)))
+        per_row = []
+        for label, fmt, N, K, W, x in self.data:  # calibration: a few rows on one thread
+            t0 = time.perf_counter()
+            oracle.gemv(fmt, x, W, N, K, 0, 4)
+            per_row.append((time.perf_counter() - t0) / 4)
+        self.row_cost = sum(per_row)  # seconds for one row of every GEMV
+
+    def run(self, budget_s: float):
+        """One timed sample costing about `budget_s` of wall time.  Returns (GB/s, s, text)."""
+        rows = max(1, int(budget_s * self.threads / max(self.row_cost, 1e-9)))
+        jobs, nbytes = [], 0
+        for label, fmt, N, K, W, x in self.data:
+            r = min(rows, N)
+            start = (N - r) // 2
+            chunk = max(1, math.ceil(r / self.threads))
+            for a in range(start, start + r, chunk):
+                jobs.append((fmt, x, W, N, K, a, min(start + r, a + chunk)))
+            nbytes += synth.packed_bytes(fmt, r, K) + 2 * K + 4 * r
+        t0 = time.perf_counter()
+        list(self.pool.map(lambda j: self.oracle.gemv(*j), jobs))
+        dt = time.perf_counter() - t0
+        sample = "middle rows of each GEMV: " + ", ".join(
+            f"{min(rows, d[2])} of {d[0]} {d[2]}x{d[3]}" for d in self.data)
+        return nbytes / dt / 1e9, dt, sample
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def run_reference(args, gemvs, rank, world):
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    sampler = OracleSampler(gemvs, threads)
+    per_step = max(0.01, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        sampler.run(per_step)
+    rates, total, sample = [], 0.0, ""
+    for _ in range(args.steps):
+        r, dt, sample = sampler.run(per_step)
+        rates.append(r)
+        total += dt
+    sampler.close()
+    value = statistics.median(rates)
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "shapes": [f"{g[0]}:{synth.FORMAT_NAMES[g[1]]}:{g[2]}x{g[3]}"
+                                                             for g in gemvs]},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"per step: {sample}"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def largest_divisor_le(k: int, cap: int) -> int:
+    for d in range(min(k, cap), 0, -1):
+        if k % d == 0:
+            return d
+    return 1
+
+
+def run_ours(args, gemvs, rank, world):
+    import torch
+
+    from quantized_weight_dequant_gb300 import qgemv
+    from quantized_weight_dequant_gb300.build import build_library
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build_library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    h = qgemv.create(local)
+    if args.pdl:
+        qgemv.set_option(h, qgemv.OPT_PDL, 1)
+
+    # Inputs: one seeded matrix per GEMV, cloned on the device into C rotating copies.
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    step_w_bytes = sum(synth.packed_bytes(f, n, k) for _, f, n, k, _ in gemvs)
+    copies = max(2, math.ceil(3 * l2 / step_w_bytes))
+    xs, Ws, ys, xbits = {}, [], [], {}
+    for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
+        seed = synth.config_seed(1, gi) + 100 * rank
+        W = synth.make_weights(fmt, N, K, seed)
+        Wd = torch.from_numpy(W).to(dev)
+        Ws.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
+        if (xk, K, fmt) not in xs:
+            xb = synth.make_x(fmt, K, seed)
+            xbits[(xk, K, fmt)] = xb
+            xs[(xk, K, fmt)] = torch.from_numpy(xb.view(np.int16).copy()).to(dev)
+        ys.append(torch.empty(N, dtype=torch.float32, device=dev))
+        del W
+    step_bytes = sum(gemv_bytes(f, n, k) for _, f, n, k, _ in gemvs)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        c = i % copies
+        for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
+            qgemv.run(h, fmt, xs[(xk, K, fmt)], Ws[gi][c], N, K, ys[gi], stream=s)
+
+    # sanity: one step, checked for errors, before anything is captured
+    with torch.cuda.stream(stream):
+        step(0, stream)
+    stream.synchronize()
+    st = qgemv.check_error(h, stream)
+    if st != qgemv.OK:
+        raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
+
+    spg = largest_divisor_le(args.steps, args.graph_steps)
+    reps = args.steps // spg
+    g = torch.cuda.CUDAGraph()
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(spg):
+            step(i, stream)
+    launches_per_step = 0
+    for _, f, n, k, _ in gemvs:
+        d = qgemv.describe(h, f, n, k)
+        split = int(d.split("splitk=")[1].split()[0]) if "splitk=" in d else 1
+        launches_per_step += 1 + (1 if split > 1 else 0)
+
+    # warm-up: at least W steps
+    warm_reps = max(1, math.ceil(args.warmup / spg))
+    with torch.cuda.stream(stream):
+        for _ in range(warm_reps):
+            g.replay()
+    stream.synchronize()
+
+    clocks = Clocks(local, str(getattr(props, "uuid", "")) or None) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    clk = clocks.stop() if clocks else None
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    st = qgemv.check_error(h, stream)
+    if st != qgemv.OK:
+        raise RuntimeError(f"qgemv error after timing: {qgemv.status_string(st)}")
+
+    value = world * args.steps * step_bytes / (elapsed_ms * 1e-3) / 1e9
+    ms_per_step = elapsed_ms / args.steps
+
+    # Per-GEMV duration (CUDA events around graph replays of R launches of one GEMV).
+    per_call = {}
+    for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
+        R = 200
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg, stream=stream):
+            for i in range(R):
+                qgemv.run(h, fmt, xs[(xk, K, fmt)], Ws[gi][i % copies], N, K, ys[gi], stream=stream)
+        with torch.cuda.stream(stream):
+            gg.replay()
+        stream.synchronize()
+        samples = []
+        for _ in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                gg.replay()
+                b.record(stream)
+            stream.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3 / R)
+        us = statistics.median(samples)
+        per_call[label] = {"us": us, "GB/s": gemv_bytes(fmt, N, K) / (us * 1e-6) / 1e9,
+                           "shape": f"{synth.FORMAT_NAMES[fmt]} {N}x{K}", "plan": qgemv.describe(h, fmt, N, K)}
+        del gg
+    dom = max(gemvs, key=lambda g_: gemv_bytes(g_[1], g_[2], g_[3]))[0]
+    peak, peak_kind = load_peaks()
+    achieved = per_call[dom]["GB/s"]
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": args.traffic, "kernel": f"stream_kernel {per_call[dom]['shape']}",
+                "peak_kind": f"hbm_gbs of {peak_kind} (copy bandwidth)",
+                "achieved_how": "algorithmic bytes per launch / mean launch duration over graph replays of 200 "
+                                "launches rotating weight copies (CUDA events on the launch stream)"}
+
+    # End to end through the public API: pinned host x -> device, 3 GEMVs, y -> pinned host.
+    e2e_steps = min(args.steps, 2000)
+    hx = {k: torch.from_numpy(v.view(np.int16).copy()).pin_memory() for k, v in xbits.items()}
+    hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in ys]
+    h2d = sum(2 * k[1] for k in hx)
+    d2h = sum(4 * y.numel() for y in ys)
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            for k in hx:
+                xs[k].copy_(hx[k], non_blocking=True)
+            step(i, stream)
+            for y, hyy in zip(ys, hy):
+                hyy.copy_(y, non_blocking=True)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(e2e_steps):
+            for k in hx:
+                xs[k].copy_(hx[k], non_blocking=True)
+            step(i, stream)
+            for y, hyy in zip(ys, hy):
+                hyy.copy_(y, non_blocking=True)
+        b.record(stream)
+    stream.synchronize()
+    e2e_ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * e2e_steps * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": e2e_ms / e2e_steps,
+           "how": "stream-ordered: pinned x H2D, qgemv_run per GEMV, y D2H per step; weights resident"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sampler = OracleSampler(gemvs, threads)
+        rate, dt, sample = sampler.run(args.cpu_seconds)
+        sampler.close()
+        cpu = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{sample}; {dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": args.workload,
+                           "shapes": [f"{g_[0]}:{synth.FORMAT_NAMES[g_[1]]}:{g_[2]}x{g_[3]}" for g_ in gemvs],
+                           "bytes_per_step": step_bytes,
+                           "l2": f"inputs larger than L2: {copies} rotating weight copies = "
+                                 f"{copies * step_w_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
+                           "timing": f"CUDA graph of {spg} steps replayed {reps}x, CUDA events",
+                           "pdl": bool(args.pdl)},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+                "us_per_call": per_call, "impl": "ours", "build": qgemv.build_marker(),
+                "gpu": props.name}
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--graph-steps", type=int, default=200)
+    ap.add_argument("--pdl", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the dominant kernel, when known for this build")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    gemvs = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, gemvs, rank, world)
+    return run_ours(args, gemvs, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,172 @@
+/*
+ * qgemv: batch-1 GEMV with block-quantised weights dequantised on the fly, for GB300
+ * (sm_103a).
+ *
+ *     y[n] = sum_k x[k] * dequant(W)[n, k],   n < N, k < K        (M = 1, alpha = 1, beta = 0)
+ *
+ * The operation is the GEMV of "Writing a high performant GEMV + dequant for Metal"
+ * (section "What is a GEMV": y = alpha x.W^T + beta C with x:(1,K), W:(M,K), alpha = 1,
+ * beta = 0; that page's M is N here) and of the Mojo "fp4_gemv" page (out = x @ dequant(W)^T
+ * at M = 1).  Weights stay in their packed block format in device memory; every kernel
+ * streams the packed bytes once, decodes them in registers and accumulates in fp32.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named x, W, y, codes, scales, mins are DEVICE pointers owned by the caller.
+ *    The library never frees, keeps or retains them past the call's stream work.
+ *  - Calls are asynchronous on `stream`; nothing is allocated and nothing synchronises
+ *    inside qgemv_run / qgemv_unpack.  Results are ready when the stream's work is done.
+ *  - Errors are reported only through the returned status; arguments are validated before
+ *    anything is launched, so an error status means no kernel was enqueued (except
+ *    QGEMV_ERR_CUDA, which means the launch itself failed).
+ *  - A handle may be used from one host thread at a time.
+ */
+#ifndef QGEMV_H_
+#define QGEMV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats.  Byte layouts (offsets inside one block, fp16 little-endian):
+ *  QGEMV_Q4_K  256 weights / 144 B: d@0, dmin@2, 12 B packed 6-bit scales+mins@4,
+ *              qs[128]@16.  w_i = d*s_g*q_i - dmin*m_g, g = i/32 (Metal GEMV page,
+ *              sections "What is a weight block?" and "Compute").  x fp16.
+ *  QGEMV_NVFP4 W4A16 (Mojo fp4_gemv page, "Structure"): E2M1 nibbles [N, K/2] (low nibble
+ *              = even k) immediately followed, in the SAME buffer, by E4M3 scales
+ *              [N, K/16]; w = e2m1 * |e4m3 scale of its 16-element block|.  x bf16.
+ *  QGEMV_TQ1_0 256 weights / 54 B: qs[48]@0 (5 base-3 digits per byte), qh[4]@48
+ *              (4 digits per byte), d@52; digit n of byte b = floor(3^(n+1) b/256) -
+ *              3 floor(3^n b/256); w = d*(t-1) ("metal: TQ1_0 kernel performance",
+ *              sections 1, 2 and "Not applicable").  x fp16.
+ *  QGEMV_Q5_K  256 weights / 176 B: d@0, dmin@2, scales[12]@4, qh[32]@16, qs[128]@48.
+ *  QGEMV_Q6_K  256 weights / 210 B: ql[128]@0, qh[64]@128, int8 scales[16]@192, d@208.
+ *  QGEMV_Q8_0   32 weights /  34 B: d@0, int8 qs[32]@2.
+ *  (Q5_K, Q6_K and Q8_0 are named on the Metal GEMV page, section "UD-Q4_K_XL"; their
+ *  standard ggml layouts are used.)  x fp16 for all of them. */
+typedef enum {
+  QGEMV_Q4_K = 0,
+  QGEMV_NVFP4 = 1,
+  QGEMV_TQ1_0 = 2,
+  QGEMV_Q5_K = 3,
+  QGEMV_Q6_K = 4,
+  QGEMV_Q8_0 = 5
+} qgemv_format_t;
+
+typedef enum {
+  QGEMV_OK = 0,
+  QGEMV_ERR_INVALID_ARG = 1,        /* null pointer / handle, bad option value */
+  QGEMV_ERR_UNSUPPORTED_FORMAT = 2, /* format id not in qgemv_format_t */
+  QGEMV_ERR_BAD_SHAPE = 3,          /* N < 1, K < 1, K not a multiple of the block length */
+  QGEMV_ERR_MISALIGNED = 4,         /* x, W or y not 16-byte aligned */
+  QGEMV_ERR_CUDA = 5,               /* a CUDA runtime call or kernel launch failed */
+  QGEMV_ERR_TIMEOUT = 6,            /* a kernel gave up on a bounded wait (see check_error) */
+  QGEMV_ERR_OOM = 7,                /* qgemv_create could not allocate its workspace */
+  QGEMV_ERR_NO_DEVICE = 8           /* no usable CUDA device / not an sm_103 device */
+} qgemv_status_t;
+
+typedef struct qgemv_handle_s* qgemv_handle_t;
+
+/* Create a handle on CUDA device `device` (made current for the call).  Queries the SM
+ * count and L2 size and allocates the handle's own device memory: the split-K partial
+ * sum workspace (fp32, sized at create time for the largest split the library chooses)
+ * and a 4-byte device error word.  *h receives the handle.  Returns QGEMV_ERR_NO_DEVICE
+ * when the device is missing or is not compute capability 10.3. */
+qgemv_status_t qgemv_create(qgemv_handle_t* h, int device);
+
+/* Free the handle's device memory and the handle.  Waits for nothing: the caller must
+ * make sure no work using the handle is still pending.  NULL is accepted. */
+qgemv_status_t qgemv_destroy(qgemv_handle_t h);
+
+/* y = x . dequant(W)^T  (overwrites y).
+ *   x        device, K elements: fp16 bits (bf16 for QGEMV_NVFP4), 16-byte aligned.
+ *   packed_W device, qgemv_packed_bytes(fmt, N, K) bytes, rows contiguous, 16-byte aligned.
+ *   y        device, N fp32 values, 16-byte aligned; must not overlap x or packed_W.
+ *   N >= 1; K >= 1 and a multiple of 256 (Q4_K, Q5_K, Q6_K, TQ1_0), 32 (Q8_0) or 16 (NVFP4).
+ * The call is asynchronous on `stream` (0 = legacy default stream), allocates nothing and
+ * does not synchronise.  Results are deterministic: the same inputs and shape give
+ * bitwise-identical y on every call (fixed reduction order, no atomics). */
+qgemv_status_t qgemv_run(qgemv_handle_t h, qgemv_format_t fmt, const void* x, const void* packed_W,
+                         int64_t N, int64_t K, float* y, cudaStream_t stream);
+
+/* Debug unpack for bit-exact checks: for every weight (n, k)
+ *     dequant(W)[n, k] = scales[n, k/G] * codes[n, k] - mins[n, k/G]      (exactly, in fp32)
+ * with G = qgemv_group_size(fmt) and
+ *   Q4_K, Q5_K: codes = q (0..15 / 0..31), scales = d*s_g, mins = dmin*m_g   (G = 32)
+ *   Q6_K:       codes = q-32 (-32..31),    scales = d*sc,    mins = 0        (G = 16)
+ *   Q8_0:       codes = int8 q,            scales = d,       mins = 0        (G = 32)
+ *   TQ1_0:      codes = t-1 (-1..1),       scales = d,       mins = 0        (G = 256)
+ *   NVFP4:      codes = 2*e2m1 (-12..12),  scales = |e4m3|/2, mins = 0       (G = 16)
+ * All scales and mins are exact in fp32.  codes: device int8 [N, K]; scales: device fp32
+ * [N, K/G]; mins: device fp32 [N, K/G] or NULL.  Same validation as qgemv_run (codes,
+ * scales, mins need no 16-byte alignment).  Asynchronous on `stream`. */
+qgemv_status_t qgemv_unpack(qgemv_handle_t h, qgemv_format_t fmt, const void* packed_W, int64_t N,
+                            int64_t K, int8_t* codes, float* scales, float* mins, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the handle's device error word.  Returns
+ * QGEMV_ERR_TIMEOUT if any kernel since the last check gave up on a bounded wait (its y
+ * is then undefined), QGEMV_ERR_CUDA if the stream reported an error, else QGEMV_OK. */
+qgemv_status_t qgemv_check_error(qgemv_handle_t h, cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* qgemv_status_string(qgemv_status_t status);
+
+/* Bytes of a packed N x K matrix in `fmt` (0 for an unknown format or a bad shape). */
+size_t qgemv_packed_bytes(qgemv_format_t fmt, int64_t N, int64_t K);
+
+/* Group length G of qgemv_unpack's scales for `fmt` (0 for an unknown format). */
+int qgemv_group_size(qgemv_format_t fmt);
+
+/* Tuning and test options (per handle).  Values are validated; bad ones give
+ * QGEMV_ERR_INVALID_ARG and change nothing.
+ *   QGEMV_OPT_FORCE_PATH      0 auto, 1 the bulk-copy streaming kernels (falls back to 0
+ *                             when the shape does not meet their alignment rule), 2 the
+ *                             plain warp-per-row kernels.
+ *   QGEMV_OPT_FORCE_SPLITK    0 auto, else the number of K slices S >= 1 of the streaming
+ *                             kernels (partials are summed by a second, fixed-order pass).
+ *   QGEMV_OPT_RING_DEPTH      0 auto, else 2..8 bulk-copy stages per warp.
+ *   QGEMV_OPT_ROWS_PER_STAGE  0 auto, else 1..8 rows per stage.
+ *   QGEMV_OPT_SPIN_LIMIT_NS   bound, in ns, of every wait on a bulk copy (default 1e9).
+ *                             0 makes any wait that does not succeed at once give up, so
+ *                             the timeout path can be tested without hanging a GPU.
+ *   QGEMV_OPT_PDL             1 launches the streaming kernels with programmatic dependent
+ *                             launch: their weight copies may start while the previous
+ *                             kernel on the stream is still running (activations are read
+ *                             only after it completes), so packed_W must not be written by
+ *                             the kernel launched just before.  0 (default) launches them
+ *                             normally.
+ *   QGEMV_OPT_TEST_STALL      test hook, default 0.  1 makes warp 0 of the first CTA of every
+ *                             streaming launch also wait on a barrier that nothing completes,
+ *                             bounded by the spin limit, so the timeout path (error word,
+ *                             draining of in-flight copies, QGEMV_ERR_TIMEOUT from
+ *                             qgemv_check_error) can be exercised without hanging a GPU. */
+typedef enum {
+  QGEMV_OPT_FORCE_PATH = 0,
+  QGEMV_OPT_FORCE_SPLITK = 1,
+  QGEMV_OPT_RING_DEPTH = 2,
+  QGEMV_OPT_ROWS_PER_STAGE = 3,
+  QGEMV_OPT_SPIN_LIMIT_NS = 4,
+  QGEMV_OPT_PDL = 5,
+  QGEMV_OPT_TEST_STALL = 6
+} qgemv_option_t;
+
+qgemv_status_t qgemv_set_option(qgemv_handle_t h, qgemv_option_t opt, int64_t value);
+
+/* Describe the launch qgemv_run would make for (fmt, N, K) into `buf` (NUL-terminated,
+ * at most `len` bytes): path, grid, block, warps per row, split, ring depth, shared
+ * memory.  Returns the same validation status as qgemv_run without launching. */
+qgemv_status_t qgemv_describe(qgemv_handle_t h, qgemv_format_t fmt, int64_t N, int64_t K, char* buf,
+                              size_t len);
+
+/* Compile-time build marker, checked by the Python binding at load (provenance). */
+const char* qgemv_build_marker(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H_ */

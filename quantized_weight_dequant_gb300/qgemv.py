@@ -1,0 +1,165 @@
+"""Python binding of libqgemv (ctypes, argument marshalling only).
+
+Every entry point has the C name without the ``qgemv_`` prefix.  Tensors are passed as
+raw device pointers (``tensor.data_ptr()``); PyTorch is used for device memory and
+streams only.  All work runs in the CUDA library; if it is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+Q4_K, NVFP4, TQ1_0, Q5_K, Q6_K, Q8_0 = 0, 1, 2, 3, 4, 5
+OPT_FORCE_PATH, OPT_FORCE_SPLITK, OPT_RING_DEPTH, OPT_ROWS_PER_STAGE, OPT_SPIN_LIMIT_NS, OPT_PDL, OPT_TEST_STALL = range(7)
+STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED_FORMAT", 3: "QGEMV_ERR_BAD_SHAPE",
+          4: "QGEMV_ERR_MISALIGNED", 5: "QGEMV_ERR_CUDA", 6: "QGEMV_ERR_TIMEOUT", 7: "QGEMV_ERR_OOM",
+          8: "QGEMV_ERR_NO_DEVICE"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_FORMAT, ERR_BAD_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
+    ERR_NO_DEVICE = range(9)
+
+EXPORTS = ["qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
+           "qgemv_status_string", "qgemv_packed_bytes", "qgemv_group_size", "qgemv_set_option",
+           "qgemv_describe", "qgemv_build_marker"]
+
+_lib = None
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree libqgemv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise ImportError(f"libqgemv.so is not built ({LIB}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB)
+        vp, i64, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.qgemv_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int]
+        L.qgemv_destroy.argtypes = [vp]
+        L.qgemv_run.argtypes = [vp, ctypes.c_int, vp, vp, i64, i64, vp, vp]
+        L.qgemv_unpack.argtypes = [vp, ctypes.c_int, vp, i64, i64, vp, vp, vp, vp]
+        L.qgemv_check_error.argtypes = [vp, vp]
+        L.qgemv_status_string.argtypes = [ctypes.c_int]
+        L.qgemv_status_string.restype = ctypes.c_char_p
+        L.qgemv_packed_bytes.argtypes = [ctypes.c_int, i64, i64]
+        L.qgemv_packed_bytes.restype = ctypes.c_size_t
+        L.qgemv_group_size.argtypes = [ctypes.c_int]
+        L.qgemv_set_option.argtypes = [vp, ctypes.c_int, i64]
+        L.qgemv_describe.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_char_p, ctypes.c_size_t]
+        L.qgemv_build_marker.restype = ctypes.c_char_p
+        for name in ("qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
+                     "qgemv_set_option", "qgemv_describe"):
+            getattr(L, name).restype = st
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise QgemvError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib().qgemv_status_string(status).decode()
+
+
+def build_marker() -> str:
+    return lib().qgemv_build_marker().decode()
+
+
+def packed_bytes(fmt: int, N: int, K: int) -> int:
+    return lib().qgemv_packed_bytes(fmt, N, K)
+
+
+def group_size(fmt: int) -> int:
+    return lib().qgemv_group_size(fmt)
+
+
+class Handle:
+    """Owns a qgemv_handle_t (split-K workspace and error word on one device)."""
+
+    def __init__(self, device: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().qgemv_create(ctypes.byref(h), device), "qgemv_create")
+        self._h = h
+        self.device = device
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().qgemv_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def create(device: int = 0) -> Handle:
+    return Handle(device)
+
+
+def destroy(h: Handle) -> None:
+    h.close()
+
+
+def run(h: Handle, fmt: int, x, packed_W, N: int, K: int, y, stream=None, check: bool = True) -> int:
+    """y = x . dequant(W)^T, asynchronous on `stream` (default: torch's current stream)."""
+    st = lib().qgemv_run(h.ptr, fmt, _ptr(x), _ptr(packed_W), N, K, _ptr(y), _stream(stream))
+    if check:
+        _check(st, "qgemv_run")
+    return st
+
+
+def unpack(h: Handle, fmt: int, packed_W, N: int, K: int, codes, scales, mins=None, stream=None,
+           check: bool = True) -> int:
+    st = lib().qgemv_unpack(h.ptr, fmt, _ptr(packed_W), N, K, _ptr(codes), _ptr(scales), _ptr(mins),
+                            _stream(stream))
+    if check:
+        _check(st, "qgemv_unpack")
+    return st
+
+
+def check_error(h: Handle, stream=None) -> int:
+    return lib().qgemv_check_error(h.ptr, _stream(stream))
+
+
+def set_option(h: Handle, opt: int, value: int, check: bool = True) -> int:
+    st = lib().qgemv_set_option(h.ptr, opt, value)
+    if check:
+        _check(st, "qgemv_set_option")
+    return st
+
+
+def describe(h: Handle, fmt: int, N: int, K: int) -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(lib().qgemv_describe(h.ptr, fmt, N, K, buf, 512), "qgemv_describe")
+    return buf.value.decode()
