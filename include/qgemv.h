@@ -72,9 +72,7 @@ typedef enum {
 typedef struct qgemv_handle_s* qgemv_handle_t;
 
 /* Create a handle on CUDA device `device` (made current for the call).  Queries the SM
- * count and L2 size and allocates the handle's own device memory: the split-K partial
- * sum workspace (fp32, sized at create time for the largest split the library chooses)
- * and a 4-byte device error word.  *h receives the handle.  Returns QGEMV_ERR_NO_DEVICE
+ * count and L2 size and allocates the handle's only device memory, a 4-byte error word.  *h receives the handle.  Returns QGEMV_ERR_NO_DEVICE
  * when the device is missing or is not compute capability 10.3. */
 qgemv_status_t qgemv_create(qgemv_handle_t* h, int device);
 
@@ -126,10 +124,9 @@ int qgemv_group_size(qgemv_format_t fmt);
  *   QGEMV_OPT_FORCE_PATH      0 auto, 1 the bulk-copy streaming kernels (falls back to 0
  *                             when the shape does not meet their alignment rule), 2 the
  *                             plain warp-per-row kernels.
- *   QGEMV_OPT_FORCE_SPLITK    0 auto, else the number of K slices S >= 1 of the streaming
- *                             kernels (partials are summed by a second, fixed-order pass).
- *   QGEMV_OPT_RING_DEPTH      0 auto, else 2..8 bulk-copy stages per warp.
- *   QGEMV_OPT_ROWS_PER_STAGE  0 auto, else 1..8 rows per stage.
+ *   QGEMV_OPT_RING_DEPTH      0 auto, else 2..8: copy stages per warp of the streaming
+ *                             kernel (2, 3, 4 or 6 are used; fewer if they do not fit).
+ *   QGEMV_OPT_ROWS_PER_STAGE  0 auto, else 1..8 rows per stage (1, 2 or 4 are used).
  *   QGEMV_OPT_SPIN_LIMIT_NS   bound, in ns, of every wait on a bulk copy (default 1e9).
  *                             0 makes any wait that does not succeed at once give up, so
  *                             the timeout path can be tested without hanging a GPU.
@@ -143,15 +140,19 @@ int qgemv_group_size(qgemv_format_t fmt);
  *                             streaming launch also wait on a barrier that nothing completes,
  *                             bounded by the spin limit, so the timeout path (error word,
  *                             draining of in-flight copies, QGEMV_ERR_TIMEOUT from
- *                             qgemv_check_error) can be exercised without hanging a GPU. */
+ *                             qgemv_check_error) can be exercised without hanging a GPU.
+ *   QGEMV_OPT_CTAS_PER_SM     streaming kernel CTAs per SM, 1 or 2 (default 2, used when
+ *                             a row needs at most 8 warps); with 1, each CTA takes about half
+ *                             an SM, so the next kernel of a programmatic-dependent-launch
+ *                             chain can start on the other half. */
 typedef enum {
   QGEMV_OPT_FORCE_PATH = 0,
-  QGEMV_OPT_FORCE_SPLITK = 1,
   QGEMV_OPT_RING_DEPTH = 2,
   QGEMV_OPT_ROWS_PER_STAGE = 3,
   QGEMV_OPT_SPIN_LIMIT_NS = 4,
   QGEMV_OPT_PDL = 5,
-  QGEMV_OPT_TEST_STALL = 6
+  QGEMV_OPT_TEST_STALL = 6,
+  QGEMV_OPT_CTAS_PER_SM = 7
 } qgemv_option_t;
 
 qgemv_status_t qgemv_set_option(qgemv_handle_t h, qgemv_option_t opt, int64_t value);

@@ -7,7 +7,8 @@
 #include <new>
 
 #include "../../include/qgemv.h"
-#include "qgemv_kernels.cuh"
+#include "qgemv_simple.cuh"
+#include "qgemv_stream.cuh"
 
 #ifndef QGEMV_BUILD_ID
 #define QGEMV_BUILD_ID "unversioned"
@@ -17,20 +18,18 @@ namespace {
 
 using namespace qg;
 
-constexpr size_t kWorkspaceBytes = 64ull << 20;  // split-K partials (fp32)
-constexpr int kMaxWarpsPerCta = 16;
-constexpr size_t kSmemBudget = 200 * 1024;       // ring + barriers + reduction buffer per CTA
-constexpr size_t kRedBudget = 16 * 1024;
+constexpr int kMaxWarps = 16;                    // per CTA (launch bound 512 threads)
+constexpr size_t kRedBudget = 16 * 1024;         // cross-warp reduction buffer per CTA
 
 struct Handle {
   int device = 0;
   int sms = 0;
   int l2_bytes = 0;
   size_t smem_optin = 0;
-  float* ws = nullptr;
   int* err = nullptr;
+  int ctas_per_sm = 2;
+  size_t dyn_smem_max[6][3] = {};
   int force_path = 0;
-  int force_splitk = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
   uint64_t spin_ns = 1000000000ull;
@@ -79,29 +78,47 @@ int group_size(int f) {
 }
 
 struct Plan {
-  int path = 2;  // 1 streaming kernels, 2 warp-per-row kernels
+  int path = 2;  // 1 streaming kernel, 2 warp-per-row kernel
   StreamArgs sa{};
-  int threads = 0, grid_x = 0, S = 1;
+  int grid = 0, threads = 0, R = 2;
   size_t smem = 0;
   int rw_grid = 0, rw_block = 256;
 };
 
-template <class Dec>
-const void* stream_fn() {
-  return reinterpret_cast<const void*>(&stream_kernel<Dec>);
-}
+}  // namespace
 
-const void* stream_kernel_for(int f) {
+namespace qg {
+const void* stream_kernel_q4k(int rows_per_item);
+const void* stream_kernel_q5k(int rows_per_item);
+const void* stream_kernel_q6k(int rows_per_item);
+const void* stream_kernel_q80(int rows_per_item);
+const void* stream_kernel_tq10(int rows_per_item);
+const void* stream_kernel_nvfp4(int rows_per_item);
+}  // namespace qg
+
+namespace {
+
+const void* stream_kernel_for(int f, int R) {
   switch (f) {
-    case F_Q4K: return stream_fn<DecQ4K>();
-    case F_Q5K: return stream_fn<DecQ5K>();
-    case F_Q6K: return stream_fn<DecQ6K>();
-    case F_Q80: return stream_fn<DecQ80>();
-    case F_TQ10: return stream_fn<DecTQ10>();
-    case F_NVFP4: return stream_fn<DecNVFP4>();
+    case F_Q4K: return stream_kernel_q4k(R);
+    case F_Q5K: return stream_kernel_q5k(R);
+    case F_Q6K: return stream_kernel_q6k(R);
+    case F_Q80: return stream_kernel_q80(R);
+    case F_TQ10: return stream_kernel_tq10(R);
+    case F_NVFP4: return stream_kernel_nvfp4(R);
   }
   return nullptr;
 }
+
+int r_index(int R) { return R == 1 ? 0 : R == 2 ? 1 : 2; }
+
+void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
+  pl.path = 2;
+  pl.rw_block = 256;
+  pl.rw_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, int64_t{h.sms} * 8)));
+}
+
+int slice_of(int f) { return 8 * sb_bytes(f) + 8 * sb_bytes2(f); }
 
 qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl) {
   const int64_t nsb = K / 256;
@@ -110,82 +127,52 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
     rb1 = (f == F_NVFP4) ? K / 2 : nsb * sb_bytes(f);
     rb2 = (f == F_NVFP4) ? K / 16 : 0;
   }
-  const bool fast_ok = (K % 256 == 0) && rb1 % 16 == 0 && rb2 % 16 == 0 && nsb <= (int64_t{1} << 30);
-  int path = fast_ok ? 1 : 2;
-  if (h.force_path == 2) path = 2;
-  pl.path = path;
-  if (path == 2) {
-    pl.rw_block = 256;
-    const int64_t want = (N + 7) / 8;
-    pl.rw_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t{h.sms} * 8)));
+  const int64_t Wk64 = (nsb + 7) / 8;
+  const bool fast_ok = (K % 256 == 0) && rb1 % 16 == 0 && rb2 % 16 == 0 && Wk64 >= 1 && Wk64 <= kMaxWarps;
+  if (!fast_ok || h.force_path == 2) {
+    rowwarp_plan(h, N, pl);
     return QGEMV_OK;
   }
-  const int wk_full = static_cast<int>((nsb + 7) / 8);
-  int S = (wk_full + kMaxWarpsPerCta - 1) / kMaxWarpsPerCta;
-  if (h.force_splitk > 0) S = std::min<int>(h.force_splitk, static_cast<int>(nsb));
-  const int sb_per_split = 8 * static_cast<int>(((nsb + S - 1) / S + 7) / 8);
-  S = static_cast<int>((nsb + sb_per_split - 1) / sb_per_split);
-  const int Wk = sb_per_split / 8;
-  const int P = std::max(1, kMaxWarpsPerCta / Wk);
+  const int Wk = static_cast<int>(Wk64);
+  const int cps = (Wk <= kMaxWarps / 2) ? h.ctas_per_sm : 1;  // CTAs per SM
+  const int P = std::max(1, (kMaxWarps / cps) / Wk);
   const int warps = P * Wk;
-  const int slice = 8 * sb_bytes(f) + 8 * sb_bytes2(f);  // multiple of 16 for every format
-  int R = h.rows_per_stage > 0 ? h.rows_per_stage : 2;
-  int D = h.ring_depth;
-  if (D == 0) {
-    D = static_cast<int>(kSmemBudget / (static_cast<size_t>(warps) * R * slice + 8));
-    D = std::min(8, D);
-    if (D < 2 && R > 1) {
-      R = 1;
-      D = std::min<int>(8, static_cast<int>(kSmemBudget / (static_cast<size_t>(warps) * slice + 8)));
-    }
-    D = std::max(2, D);
-  }
-  // Grid: one wave of CTAs over the rows, enough CTAs that the reduction buffer fits.
-  const int64_t sms = h.sms;
-  int64_t grid = std::min<int64_t>((N + P - 1) / P, std::max<int64_t>(1, sms / S));
-  if (Wk > 1) {
-    const int64_t max_rows = static_cast<int64_t>(kRedBudget / (4 * static_cast<size_t>(Wk)));
-    grid = std::max<int64_t>(grid, (N + max_rows - 1) / max_rows);
-  }
+  int64_t grid = std::min<int64_t>(int64_t{h.sms} * cps, (N + P - 1) / P);
+  if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
   grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
-  if (static_cast<int64_t>(S) * N * 4 > static_cast<int64_t>(kWorkspaceBytes) && S > 1) {
-    pl.path = 2;  // would not fit the handle's workspace: plain path instead
-    pl.rw_block = 256;
-    pl.rw_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, int64_t{h.sms} * 8)));
+  const int red_rows = static_cast<int>((N + grid - 1) / grid + 1);
+  const int slice = slice_of(f);
+  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : 2;
+  int D = h.ring_depth > 0 ? (h.ring_depth >= 6 ? 6 : h.ring_depth) : 4;
+  const size_t limit = std::min(h.dyn_smem_max[f][r_index(R)], static_cast<size_t>((228 * 1024) / cps - 1024));
+  auto smem_of = [&](int d, int r) { return stream_smem_bytes(warps, d, r, slice, Wk, red_rows); };
+  while (smem_of(D, R) > limit && (D > 2 || R > 1)) {
+    if (D > 2)
+      D = (D == 6) ? 4 : D - 1;
+    else
+      R >>= 1, D = 4;
+  }
+  const size_t smem = smem_of(D, R);
+  if (smem > std::min(limit, h.dyn_smem_max[f][r_index(R)])) {
+    rowwarp_plan(h, N, pl);
     return QGEMV_OK;
   }
-  const int red_rows = static_cast<int>((N + grid - 1) / grid + 1);
-  // Forced ring shapes are upper bounds: shrink depth, then rows per stage, to fit.
-  size_t smem = stream_smem_bytes(warps, D, R * slice, Wk, red_rows);
-  while (smem > h.smem_optin && (D > 2 || R > 1)) {
-    if (D > 2)
-      --D;
-    else
-      --R;
-    smem = stream_smem_bytes(warps, D, R * slice, Wk, red_rows);
-  }
-  if (smem > h.smem_optin) return QGEMV_ERR_BAD_SHAPE;
-
   StreamArgs& a = pl.sa;
   a.N = N;
   a.row_bytes = rb1;
   a.row_bytes2 = rb2;
   a.nsb = static_cast<int>(nsb);
-  a.sb_per_split = sb_per_split;
   a.Wk = Wk;
   a.P = P;
-  a.R = R;
   a.D = D;
-  a.slot_bytes = R * slice;
-  a.slice_stride = slice;
   a.red_rows = red_rows;
   a.err = h.err;
   a.spin_ns = h.spin_ns;
   a.test_stall = h.test_stall;
-  a.pdl = h.pdl;
+  pl.path = 1;
+  pl.grid = static_cast<int>(grid);
   pl.threads = 32 * warps;
-  pl.grid_x = static_cast<int>(grid);
-  pl.S = S;
+  pl.R = R;
   pl.smem = smem;
   return QGEMV_OK;
 }
@@ -269,24 +256,34 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
   h->sms = prop.multiProcessorCount;
   h->l2_bytes = prop.l2CacheSize;
   h->smem_optin = prop.sharedMemPerBlockOptin;
-  if (cudaMalloc(&h->ws, kWorkspaceBytes) != cudaSuccess || cudaMalloc(&h->err, sizeof(int)) != cudaSuccess ||
-      cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) {
+  auto release = [h]() {
     cudaGetLastError();
-    cudaFree(h->ws);
     cudaFree(h->err);
     delete h;
+  };
+  if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) {
+    release();
     return QGEMV_ERR_OOM;
   }
-  for (int f = 0; f <= 5; ++f) {
-    if (cudaFuncSetAttribute(stream_kernel_for(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(h->smem_optin)) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(h->ws);
-      cudaFree(h->err);
-      delete h;
-      return QGEMV_ERR_CUDA;
-    }
+  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    release();
+    return QGEMV_ERR_CUDA;
   }
+  for (int f = 0; f <= 5; ++f)
+    for (int R : {1, 2, 4}) {
+      cudaFuncAttributes fa;
+      const void* fn = stream_kernel_for(f, R);
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+        release();
+        return QGEMV_ERR_CUDA;
+      }
+      size_t& mx = h->dyn_smem_max[f][r_index(R)];
+      mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
+        release();
+        return QGEMV_ERR_CUDA;
+      }
+    }
   *out = reinterpret_cast<qgemv_handle_t>(h);
   return QGEMV_OK;
 }
@@ -294,7 +291,6 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
 qgemv_status_t qgemv_destroy(qgemv_handle_t hh) {
   Handle* h = reinterpret_cast<Handle*>(hh);
   if (!h) return QGEMV_OK;
-  cudaFree(h->ws);
   cudaFree(h->err);
   delete h;
   return QGEMV_OK;
@@ -307,10 +303,6 @@ qgemv_status_t qgemv_set_option(qgemv_handle_t hh, qgemv_option_t opt, int64_t v
     case QGEMV_OPT_FORCE_PATH:
       if (v < 0 || v > 2) return QGEMV_ERR_INVALID_ARG;
       h->force_path = static_cast<int>(v);
-      return QGEMV_OK;
-    case QGEMV_OPT_FORCE_SPLITK:
-      if (v < 0 || v > 4096) return QGEMV_ERR_INVALID_ARG;
-      h->force_splitk = static_cast<int>(v);
       return QGEMV_OK;
     case QGEMV_OPT_RING_DEPTH:
       if (v != 0 && (v < 2 || v > 8)) return QGEMV_ERR_INVALID_ARG;
@@ -332,6 +324,10 @@ qgemv_status_t qgemv_set_option(qgemv_handle_t hh, qgemv_option_t opt, int64_t v
       if (v < 0 || v > 1) return QGEMV_ERR_INVALID_ARG;
       h->test_stall = static_cast<int>(v);
       return QGEMV_OK;
+    case QGEMV_OPT_CTAS_PER_SM:
+      if (v < 1 || v > 2) return QGEMV_ERR_INVALID_ARG;
+      h->ctas_per_sm = static_cast<int>(v);
+      return QGEMV_OK;
   }
   return QGEMV_ERR_INVALID_ARG;
 }
@@ -346,9 +342,8 @@ qgemv_status_t qgemv_describe(qgemv_handle_t hh, qgemv_format_t fmt, int64_t N, 
   if (buf && len) {
     if (pl.path == 1)
       snprintf(buf, len,
-               "path=stream grid=%dx%d block=%d warps_per_row=%d row_groups=%d rows_per_stage=%d ring=%d "
-               "splitk=%d smem=%zu pdl=%d",
-               pl.grid_x, pl.S, pl.threads, pl.sa.Wk, pl.sa.P, pl.sa.R, pl.sa.D, pl.S, pl.smem, pl.sa.pdl);
+               "path=stream grid=%d block=%d kcols=%d row_groups=%d rows_per_stage=%d ring=%d smem=%zu pdl=%d",
+               pl.grid, pl.threads, pl.sa.Wk, pl.sa.P, pl.R, pl.sa.D, pl.smem, h->pdl);
     else
       snprintf(buf, len, "path=rowwarp grid=%d block=%d", pl.rw_grid, pl.rw_block);
   }
@@ -375,9 +370,9 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
   a.W = Wb;
   a.W2 = (fmt == QGEMV_NVFP4) ? Wb + N * (K / 2) : nullptr;
   a.x = static_cast<const uint16_t*>(x);
-  a.out = (pl.S > 1) ? h->ws : y;
+  a.y = y;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.grid_x, pl.S, 1);
+  cfg.gridDim = dim3(pl.grid, 1, 1);
   cfg.blockDim = dim3(pl.threads, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
@@ -389,14 +384,9 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
     cfg.numAttrs = 1;
   }
   void* args[] = {&a};
-  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt), args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt, pl.R), args) != cudaSuccess) {
     cudaGetLastError();
     return QGEMV_ERR_CUDA;
-  }
-  if (pl.S > 1) {
-    const int grid = static_cast<int>(std::min<int64_t>((N + 255) / 256, int64_t{h->sms} * 4));
-    splitk_reduce<<<grid, 256, 0, stream>>>(h->ws, y, N, pl.S);
-    if (cudaGetLastError() != cudaSuccess) return QGEMV_ERR_CUDA;
   }
   return QGEMV_OK;
 }

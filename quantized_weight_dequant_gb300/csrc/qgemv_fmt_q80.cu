@@ -1,0 +1,15 @@
+// Streaming-kernel instantiations for one weight format (compiled on their own so the
+// library's translation units build in parallel).
+#include "qgemv_stream.cuh"
+
+namespace qg {
+
+const void* stream_kernel_q80(int rows_per_item) {
+  switch (rows_per_item) {
+    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecQ80, 1>);
+    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecQ80, 2>);
+    default: return reinterpret_cast<const void*>(&stream_kernel<DecQ80, 4>);
+  }
+}
+
+}  // namespace qg

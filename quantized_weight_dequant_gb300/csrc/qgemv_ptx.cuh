@@ -46,6 +46,10 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -58,20 +62,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_try_wait, but a thread that finds the phase incomplete is suspended (not
+// spinning, so it takes no issue slots from other warps) until the phase completes or
+// `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 
-// Waits for phase `parity` of `bar` to complete, for at most `limit_ns` nanoseconds after
-// the first unsuccessful probe.  Returns false when it gave up.
+// Waits for phase `parity` of `bar` to complete, giving up once about `limit_ns` have
+// passed after the first unsuccessful probe (measured in SM cycles, counted as 4 per ns so
+// the bound holds at any clock up to 4 GHz).  The waiting thread sleeps in the probe.
+// Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = clock64();
+  const long long limit = static_cast<long long>(limit_ns < (1ull << 60) ? limit_ns : (1ull << 60)) * 4;
+  const uint32_t hint = static_cast<uint32_t>(limit_ns < 1000000ull ? limit_ns : 1000000ull);
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 >= limit_ns) return false;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (clock64() - t0 >= limit) return false;
   }
 }
 

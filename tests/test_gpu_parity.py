@@ -38,7 +38,8 @@ def _check_full(h, fmt, N, K, seed, what=""):
 
 # Small and mid shapes: several tiles, ragged tails, both paths.
 SHAPES = {
-    synth.Q4_K: [(1, 256), (3, 512), (37, 4096), (300, 2304), (64, 14336), (1024, 1024), (131, 6400), (5, 36864)],
+    synth.Q4_K: [(1, 256), (3, 512), (37, 4096), (300, 2304), (64, 14336), (1024, 1024), (131, 6400), (5, 36864),
+                 (2, 32768)],
     synth.Q5_K: [(1, 256), (33, 4096), (70, 2560), (16, 12288)],
     synth.Q6_K: [(1, 256), (9, 768), (40, 4096), (17, 12288), (5, 2048)],
     synth.Q8_0: [(1, 32), (3, 160), (50, 4096), (8, 12288), (2, 288)],
@@ -80,16 +81,17 @@ def test_plain_row_path_matches_oracle(h, fmt, N, K):
         qgemv.set_option(h, qgemv.OPT_FORCE_PATH, 0)
 
 
-@pytest.mark.parametrize("S", [2, 3, 7])
+@pytest.mark.parametrize("cps,pdl", [(1, 0), (1, 1), (2, 1)])
 @pytest.mark.parametrize("fmt", [synth.Q4_K, synth.NVFP4, synth.Q6_K])
-def test_split_k_matches_oracle(h, fmt, S):
-    N, K = 70, 14336
-    qgemv.set_option(h, qgemv.OPT_FORCE_SPLITK, S)
+def test_launch_variants_match_oracle(h, fmt, cps, pdl):
+    qgemv.set_option(h, qgemv.OPT_CTAS_PER_SM, cps)
+    qgemv.set_option(h, qgemv.OPT_PDL, pdl)
     try:
-        assert f"splitk={S}" in qgemv.describe(h, fmt, N, K)
-        _check_full(h, fmt, N, K, seed=11 * S + fmt, what=f"split {S}")
+        _check_full(h, fmt, 70, 14336, seed=11 * cps + pdl + fmt, what=f"cps={cps} pdl={pdl}")
+        _check_full(h, fmt, 333, 4096, seed=13 * cps + pdl + fmt, what=f"cps={cps} pdl={pdl}")
     finally:
-        qgemv.set_option(h, qgemv.OPT_FORCE_SPLITK, 0)
+        qgemv.set_option(h, qgemv.OPT_CTAS_PER_SM, 2)
+        qgemv.set_option(h, qgemv.OPT_PDL, 0)
 
 
 @pytest.mark.parametrize("depth,rows", [(2, 1), (3, 3), (8, 2), (4, 8)])
