@@ -121,15 +121,17 @@ int qgemv_group_size(qgemv_format_t fmt);
 
 /* Tuning and test options (per handle).  Values are validated; bad ones give
  * QGEMV_ERR_INVALID_ARG and change nothing.
- *   QGEMV_OPT_FORCE_PATH      0 auto, 1 the bulk-copy streaming kernels (falls back to 0
+ *   QGEMV_OPT_FORCE_PATH      0 auto, 1 the cp.async streaming kernels (falls back to 0
  *                             when the shape does not meet their alignment rule), 2 the
  *                             plain warp-per-row kernels.
  *   QGEMV_OPT_RING_DEPTH      0 auto, else 2..8: copy stages per warp of the streaming
- *                             kernel (2, 3, 4 or 6 are used; fewer if they do not fit).
+ *                             kernel (2, 3 or 4 are used, larger values mean 4; fewer
+ *                             if they do not fit in shared memory).
  *   QGEMV_OPT_ROWS_PER_STAGE  0 auto, else 1..8 rows per stage (1, 2 or 4 are used).
- *   QGEMV_OPT_SPIN_LIMIT_NS   bound, in ns, of every wait on a bulk copy (default 1e9).
- *                             0 makes any wait that does not succeed at once give up, so
- *                             the timeout path can be tested without hanging a GPU.
+ *   QGEMV_OPT_SPIN_LIMIT_NS   bound, in ns, of every spin-wait on a barrier in the kernels
+ *                             (default 1e9); 0 makes such a wait give up at once.  (The
+ *                             streaming kernel waits for its own copies with
+ *                             cp.async.wait_group, which the hardware completes.)
  *   QGEMV_OPT_PDL             1 launches the streaming kernels with programmatic dependent
  *                             launch: their weight copies may start while the previous
  *                             kernel on the stream is still running (activations are read

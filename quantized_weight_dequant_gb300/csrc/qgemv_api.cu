@@ -28,7 +28,7 @@ struct Handle {
   size_t smem_optin = 0;
   int* err = nullptr;
   int ctas_per_sm = 2;
-  size_t dyn_smem_max[6][3] = {};
+  size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -80,7 +80,7 @@ int group_size(int f) {
 struct Plan {
   int path = 2;  // 1 streaming kernel, 2 warp-per-row kernel
   StreamArgs sa{};
-  int grid = 0, threads = 0, R = 2;
+  int grid = 0, threads = 0, R = 2, D = 4;
   size_t smem = 0;
   int rw_grid = 0, rw_block = 256;
 };
@@ -88,29 +88,30 @@ struct Plan {
 }  // namespace
 
 namespace qg {
-const void* stream_kernel_q4k(int rows_per_item);
-const void* stream_kernel_q5k(int rows_per_item);
-const void* stream_kernel_q6k(int rows_per_item);
-const void* stream_kernel_q80(int rows_per_item);
-const void* stream_kernel_tq10(int rows_per_item);
-const void* stream_kernel_nvfp4(int rows_per_item);
+const void* stream_kernel_q4k(int R, int D);
+const void* stream_kernel_q5k(int R, int D);
+const void* stream_kernel_q6k(int R, int D);
+const void* stream_kernel_q80(int R, int D);
+const void* stream_kernel_tq10(int R, int D);
+const void* stream_kernel_nvfp4(int R, int D);
 }  // namespace qg
 
 namespace {
 
-const void* stream_kernel_for(int f, int R) {
+const void* stream_kernel_for(int f, int R, int D) {
   switch (f) {
-    case F_Q4K: return stream_kernel_q4k(R);
-    case F_Q5K: return stream_kernel_q5k(R);
-    case F_Q6K: return stream_kernel_q6k(R);
-    case F_Q80: return stream_kernel_q80(R);
-    case F_TQ10: return stream_kernel_tq10(R);
-    case F_NVFP4: return stream_kernel_nvfp4(R);
+    case F_Q4K: return stream_kernel_q4k(R, D);
+    case F_Q5K: return stream_kernel_q5k(R, D);
+    case F_Q6K: return stream_kernel_q6k(R, D);
+    case F_Q80: return stream_kernel_q80(R, D);
+    case F_TQ10: return stream_kernel_tq10(R, D);
+    case F_NVFP4: return stream_kernel_nvfp4(R, D);
   }
   return nullptr;
 }
 
 int r_index(int R) { return R == 1 ? 0 : R == 2 ? 1 : 2; }
+int d_index(int D) { return D - 2; }
 
 void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
   pl.path = 2;
@@ -140,39 +141,47 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   int64_t grid = std::min<int64_t>(int64_t{h.sms} * cps, (N + P - 1) / P);
   if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
   grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
+  if (N / grid >= 0x7ffffffe) {  // per-CTA row counts are 32-bit in the kernel
+    rowwarp_plan(h, N, pl);
+    return QGEMV_OK;
+  }
   const int red_rows = static_cast<int>((N + grid - 1) / grid + 1);
   const int slice = slice_of(f);
   int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : 2;
-  int D = h.ring_depth > 0 ? (h.ring_depth >= 6 ? 6 : h.ring_depth) : 4;
-  const size_t limit = std::min(h.dyn_smem_max[f][r_index(R)], static_cast<size_t>((228 * 1024) / cps - 1024));
-  auto smem_of = [&](int d, int r) { return stream_smem_bytes(warps, d, r, slice, Wk, red_rows); };
-  while (smem_of(D, R) > limit && (D > 2 || R > 1)) {
+  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : 4;
+  const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
+  auto limit = [&](int d, int r) { return std::min(h.dyn_smem_max[f][r_index(r)][d_index(d)], cap); };
+  auto smem_of = [&](int d, int r) { return stream_smem(warps, d, r, slice, Wk, red_rows, static_cast<int>(K)).total; };
+  while (smem_of(D, R) > limit(D, R) && (D > 2 || R > 1)) {
     if (D > 2)
-      D = (D == 6) ? 4 : D - 1;
+      --D;
     else
       R >>= 1, D = 4;
   }
   const size_t smem = smem_of(D, R);
-  if (smem > std::min(limit, h.dyn_smem_max[f][r_index(R)])) {
+  if (smem > limit(D, R)) {
     rowwarp_plan(h, N, pl);
     return QGEMV_OK;
   }
   StreamArgs& a = pl.sa;
   a.N = N;
+  a.rows_q = static_cast<int>(N / grid);
+  a.rows_rem = static_cast<int>(N % grid);
   a.row_bytes = rb1;
   a.row_bytes2 = rb2;
   a.nsb = static_cast<int>(nsb);
   a.Wk = Wk;
   a.P = P;
-  a.D = D;
   a.red_rows = red_rows;
   a.err = h.err;
   a.spin_ns = h.spin_ns;
   a.test_stall = h.test_stall;
+  a.pdl = h.pdl;
   pl.path = 1;
   pl.grid = static_cast<int>(grid);
   pl.threads = 32 * warps;
   pl.R = R;
+  pl.D = D;
   pl.smem = smem;
   return QGEMV_OK;
 }
@@ -270,14 +279,15 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
     return QGEMV_ERR_CUDA;
   }
   for (int f = 0; f <= 5; ++f)
-    for (int R : {1, 2, 4}) {
+    for (int R : {1, 2, 4})
+      for (int D : {2, 3, 4}) {
       cudaFuncAttributes fa;
-      const void* fn = stream_kernel_for(f, R);
+      const void* fn = stream_kernel_for(f, R, D);
       if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
         release();
         return QGEMV_ERR_CUDA;
       }
-      size_t& mx = h->dyn_smem_max[f][r_index(R)];
+      size_t& mx = h->dyn_smem_max[f][r_index(R)][d_index(D)];
       mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
         release();
@@ -343,7 +353,7 @@ qgemv_status_t qgemv_describe(qgemv_handle_t hh, qgemv_format_t fmt, int64_t N, 
     if (pl.path == 1)
       snprintf(buf, len,
                "path=stream grid=%d block=%d kcols=%d row_groups=%d rows_per_stage=%d ring=%d smem=%zu pdl=%d",
-               pl.grid, pl.threads, pl.sa.Wk, pl.sa.P, pl.R, pl.sa.D, pl.smem, h->pdl);
+               pl.grid, pl.threads, pl.sa.Wk, pl.sa.P, pl.R, pl.D, pl.smem, h->pdl);
     else
       snprintf(buf, len, "path=rowwarp grid=%d block=%d", pl.rw_grid, pl.rw_block);
   }
@@ -384,7 +394,7 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
     cfg.numAttrs = 1;
   }
   void* args[] = {&a};
-  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt, pl.R), args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt, pl.R, pl.D), args) != cudaSuccess) {
     cudaGetLastError();
     return QGEMV_ERR_CUDA;
   }

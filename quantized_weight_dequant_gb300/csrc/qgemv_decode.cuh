@@ -3,19 +3,25 @@
 // Work split: a row is cut into 256-element superblocks (one Q4_K / Q5_K / Q6_K / TQ1_0
 // block, eight Q8_0 blocks, or 256 NVFP4 elements with their 16 scales) and into K-columns
 // of 8 superblocks (2048 elements).  A warp owns one K-column; lane L = 4*col + c owns
-// piece c (64 elements) of superblock col.  The lane loads the activations of its piece
-// once (two runs of 32 contiguous values) and keeps them in 32 registers of f16 pairs, in
-// the order its decode consumes them, plus the activation sums its offsets need.
+// piece c (64 elements) of superblock col.
 //
-// Exact decode with mixed-precision FMAs (sm_100+ `fma.rn.f32.f16`): a small integer v
-// stored in the low 10 bits of a 16-bit half is the f16 subnormal v * 2^-24, so masking
-// two fields into the two halves of a 32-bit register (one LOP3 per pair) gives two
-// operands whose product with an f16 activation is exact in fp32.  The 2^-24 (and the
-// 2^4 of a field sitting four bits up) is removed once per block.  This is the GPU form
-// of the Q4_K page's "multiply by the masked but unshifted nibble and correct once at
-// the end" ("Writing a high performant GEMV + dequant for Metal", section "Compute").
-// Block scales are combined the same way: d (f16) times a 6-bit scale placed as a
-// subnormal gives d*s*2^-24 in one instruction, without integer-to-float conversion.
+// Activations: the CTA first stages x in shared memory once, converted piece by piece (8
+// elements) into the form the decoders consume (stage_piece); each lane then copies the
+// two 32-element runs of its piece into 32 registers (two values each) and keeps them for
+// the whole kernel, together with the per-chunk factors and sums its offsets need.
+//
+// Integer-code formats (Q4_K, Q5_K, Q6_K, Q8_0): the codes of a row piece are byte
+// vectors (masked or assembled in place, never shifted down to one code per register)
+// and their dot product with the activations, held as 16-bit fixed point, is taken four
+// bytes at a time by dp2a into int32; the group scale, the group minimum times the
+// activation sum, and the fixed-point exponent are applied once per group.  This is the
+// GPU form of the Q4_K page's "multiply by the masked nibbles and correct once per
+// block" ("Writing a high performant GEMV + dequant for Metal", section "Compute").
+// Block scales use mixed-precision FMAs (sm_100+ `fma.rn.f32.f16`): a small integer v in
+// the low 10 bits of a 16-bit half is the f16 subnormal v * 2^-24, so d (f16) times a
+// 6-bit scale placed there is d*s*2^-24, exact, in one instruction.
+// NVFP4 decodes E2M1/E4M3 with the hardware f16 conversions and accumulates f16 x f16
+// products exactly in fp32; TQ1_0 extracts base-3 digits with one rounding FMA each.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -36,7 +42,6 @@ __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpr
 __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
 
 constexpr float kTwo24 = 16777216.0f;
-constexpr float kTwo48 = 281474976710656.0f;
 
 // c0 += lo(x2) * lo(q2); c1 += hi(x2) * hi(q2)   (f16 x f16 -> exact product, f32 accumulate)
 __device__ __forceinline__ void fma2h(float& c0, float& c1, uint32_t x2, uint32_t q2) {
@@ -45,14 +50,6 @@ __device__ __forceinline__ void fma2h(float& c0, float& c1, uint32_t x2, uint32_
       "fma.rn.f32.f16 %0, xl, ql, %0;\n\tfma.rn.f32.f16 %1, xh, qh, %1;\n\t}"
       : "+f"(c0), "+f"(c1)
       : "r"(x2), "r"(q2));
-}
-// (lo(a) * lo(b), hi(a) * hi(b)) in fp32, exact for f16 inputs.
-__device__ __forceinline__ void mul2h(float& r0, float& r1, uint32_t a2, uint32_t b2) {
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-      "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
-      "fma.rn.f32.f16 %0, al, bl, 0f00000000;\n\tfma.rn.f32.f16 %1, ah, bh, 0f00000000;\n\t}"
-      : "=f"(r0), "=f"(r1)
-      : "r"(a2), "r"(b2));
 }
 // lo(a) * (lo(b), hi(b))
 __device__ __forceinline__ void mul1x2h(float& r0, float& r1, uint32_t a2, uint32_t b2) {
@@ -63,74 +60,142 @@ __device__ __forceinline__ void mul1x2h(float& r0, float& r1, uint32_t a2, uint3
       : "r"(a2), "r"(b2));
 }
 
-// Bytes 0 and 1 of v into the low bytes of the two halves: [v.b0, 0, v.b1, 0].
-__device__ __forceinline__ uint32_t spread01(uint32_t v) { return __byte_perm(v, 0u, 0x4140u); }
+// ------------------------------------------------------------------- activation staging
+// The CTA's copy of x in shared memory: q[K] 16-bit values, e[K/32] one float per 32-element
+// chunk, s[K/16] one int per 16-element half chunk (what they hold depends on the format).
+struct XStage {
+  uint16_t* q;
+  float* e;
+  int* s;
+};
 
-// ------------------------------------------------------------------- activation loader
-// Decoders describe their x registers by: run0(c), run1(c) = superblock offsets of the two
-// 32-element runs of lane piece c; xloc(k, h) in [0, 64) = which of those 64 values is
-// half h of register k (run0 values first); xsum(k, h) = which sum the value enters
-// (-1: none), and xsum_scale() the factor the sums are stored with.
-__device__ __forceinline__ void load_runs(const uint16_t* __restrict__ x, int64_t base0, int64_t base1, bool active,
-                                          uint32_t (&v)[32]) {
-  if (active) {
-    const uint4* p0 = reinterpret_cast<const uint4*>(x + base0);
-    const uint4* p1 = reinterpret_cast<const uint4*>(x + base1);
+// d = c + a.h0 * b.b0 + a.h1 * b.b1 (lo) / a.h0 * b.b2 + a.h1 * b.b3 (hi); a two int16,
+// b four bytes (unsigned or signed).
+__device__ __forceinline__ int dp2a_lo_u(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_u(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_lo_s(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_s(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// max of the two unsigned 16-bit halves, lane-wise (sm_90+)
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void ld_chunk(const uint16_t* q, uint32_t (&v)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(q);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 a = __ldg(p0 + i), b = __ldg(p1 + i);
-      v[4 * i] = a.x, v[4 * i + 1] = a.y, v[4 * i + 2] = a.z, v[4 * i + 3] = a.w;
-      v[16 + 4 * i] = b.x, v[16 + 4 * i + 1] = b.y, v[16 + 4 * i + 2] = b.z, v[16 + 4 * i + 3] = b.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0u;
+  for (int i = 0; i < 4; ++i) {
+    const uint4 a = p[i];
+    v[4 * i] = a.x, v[4 * i + 1] = a.y, v[4 * i + 2] = a.z, v[4 * i + 3] = a.w;
   }
 }
-__device__ __forceinline__ uint32_t half_of(const uint32_t (&v)[32], int i) { return (v[i >> 1] >> (16 * (i & 1))) & 0xFFFFu; }
+// Activations are staged in 16-byte pieces of 8 values: piece i of x is loaded by one
+// thread, and the four pieces of a 32-element chunk sit in four adjacent lanes of a warp
+// (i & 3 == lane & 3), which share the chunk's largest magnitude by two shuffles.
+__device__ __forceinline__ uint32_t chunk_max_mag(const uint4& v) {
+  uint32_t m2 = vmax_u16x2(vmax_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), vmax_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  return max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+}
 
-template <class D>
-__device__ __forceinline__ void load_x_f16(D& d, const uint16_t* __restrict__ x, int64_t sb, int c, bool active) {
-  uint32_t v[32];
-  load_runs(x, sb * 256 + D::run0(c), sb * 256 + D::run1(c), active, v);
-  float sums[4] = {0.f, 0.f, 0.f, 0.f};
+// Integer-code formats: a chunk of 32 fp16 activations becomes 16-bit fixed point
+// x_i = round(x * 2^e), e chosen per chunk so that its largest |x| lands in [2^14, 2^15).
+// Values within a factor 16 of that largest one convert exactly (fp16 has 11 significant
+// bits); smaller ones are rounded with error at most 2^-15 of it.  Dot products with the
+// integer codes are then exact int32 sums (dp2a), and the code term and the group-minimum
+// term of a block use the same x_i.
+//  * Conversion is one mixed-precision FMA per value: x (f16) * 2^e1 (f16) + M (f32) with
+//    M = 1.5 * 2^(23 - (e - e1)), whose ulp is 2^(e1 - e), so the sum is rounded to
+//    nearest-even at exactly x * 2^e; its low 16 mantissa bits are then x_i in two's
+//    complement (|x_i| < 2^15 keeps the sum inside M's binade).  e1 = min(e, 15) keeps
+//    the f16 multiplier representable.
+//  * e[chunk] = 2^-e * 2^24 (the 2^24 undoes the subnormal scale factors of the decoders);
+//    s[2 chunk + h] = sum of x_i over half h, by dp2a against byte weights (1, 1).
+__device__ __forceinline__ void int_stage_piece(uint4 v, int i, const XStage& X) {
+  const int e5 = static_cast<int>(chunk_max_mag(v) >> 10);  // f16 biased exponent
+  const int e = 29 - min(e5, 30);                             // in [-1, 29]
+  const int e1 = min(e, 15);
+  const uint32_t s1 = static_cast<uint32_t>(e1 + 15) << 10;  // f16 2^e1
+  const uint32_t s2 = s1 | (s1 << 16);
+  const float M = 1.5f * p2(23 - (e - e1));
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int hs = 0;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const uint32_t lo = half_of(v, D::xloc(k, 0)), hi = half_of(v, D::xloc(k, 1));
-    d.xr[k] = lo | (hi << 16);
+  for (int k = 0; k < 4; ++k) {
+    float f0 = M, f1 = M;
+    fma2h(f0, f1, w[k], s2);
+    w[k] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
+    hs = dp2a_lo_u(w[k], 0x0101u, hs);
+  }
+  hs += __shfl_xor_sync(0xffffffffu, hs, 1);
+  reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  if ((i & 1) == 0) X.s[i >> 1] = hs;
+  if ((i & 3) == 0) X.e[i >> 2] = p2(24 - e);
+}
+
+// Lane registers of an integer-code decoder: runs run0 (registers 0..15) and run1 (16..31)
+// of its piece, the factors of their chunks and the four half-chunk sums (run0 halves,
+// then run1 halves).
+struct IntX {
+  uint32_t xr[32];
+  float xf0, xf1;
+  int xsi[4];
+
+  __device__ __forceinline__ void load(const XStage& X, int k0, int k1, bool active) {
+    if (active) {
+      uint32_t a[16], b[16];
+      ld_chunk(X.q + k0, a);
+      ld_chunk(X.q + k1, b);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int si = D::xsum(k, h);
-      if (si >= 0) sums[si] += h2f(h ? hi : lo);
+      for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
+      xf0 = X.e[k0 >> 5];
+      xf1 = X.e[k1 >> 5];
+      xsi[0] = X.s[k0 >> 4], xsi[1] = X.s[(k0 >> 4) + 1];
+      xsi[2] = X.s[k1 >> 4], xsi[3] = X.s[(k1 >> 4) + 1];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xr[i] = 0u;
+      xf0 = xf1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) xsi[m] = 0;
     }
   }
-#pragma unroll
-  for (int m = 0; m < 4; ++m) d.xs[m] = sums[m] * D::xsum_scale();
-}
+};
 
 // ------------------------------------------------------------------------------- Q4_K
-// Lane piece c = quant bytes [32c, 32c+32): low nibbles are elements 64c + t (group
-// 2c), high nibbles 64c + 32 + t (group 2c+1).  For quant word u (bytes t..t+3, t = 4u)
-// the four registers are x pairs (t, t+2), (t+1, t+3), (32+t, 34+t), (33+t, 35+t),
-// matching the masks 0x000F000F and 0x00F000F0 on the word and on the word >> 8.
-struct DecQ4K {
+// Lane piece c = quant bytes [32c, 32c+32): low nibbles are elements 64c + t (group 2c),
+// high nibbles 64c + 32 + t (group 2c+1).  For quant word u (bytes t..t+3, t = 4u) the
+// four low nibbles (word & 0x0F0F0F0F) and the four high nibbles ((word >> 4) & same)
+// are byte vectors that dp2a multiplies with activation pairs (t, t+1), (t+2, t+3) and
+// (32+t, 33+t), (34+t, 35+t): the GPU form of "multiply by the masked nibbles and correct
+// once per block" of the Q4_K page (section "Compute").  Group scales: d (f16) times a
+// 6-bit scale placed as an f16 subnormal gives d*s*2^-24 in one instruction.
+struct DecQ4K : IntX {
   static constexpr int kSB = 144, kSB2 = 0;
-  static constexpr bool kBf16X = false;
-  uint32_t xr[32];
-  float xs[4];  // xs[0] = 2^24 * sum of low-nibble x, xs[1] = 2^24 * sum of high-nibble x
   int c;
   uint32_t sel_s, sel_h, m1, m2, shm;
+  float xs0, xs1;  // activation sums of the two groups
 
-  __device__ __forceinline__ static int run0(int c) { return 64 * c; }
-  __device__ __forceinline__ static int run1(int c) { return 64 * c + 32; }
-  __device__ __forceinline__ static constexpr int xloc(int k, int h) {
-    return 4 * (k >> 2) + ((k & 3) == 1 || (k & 3) == 3 ? 1 : 0) + ((k & 3) >= 2 ? 32 : 0) + 2 * h;
-  }
-  __device__ __forceinline__ static constexpr int xsum(int k, int) { return (k & 3) < 2 ? 0 : 1; }
-  __device__ __forceinline__ static float xsum_scale() { return kTwo24; }
-  __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t sb, int c_, bool active) {
-    load_x_f16(*this, x, sb, c_, active);
-  }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
 
   __device__ __forceinline__ void init(int c_) {
     c = c_;
@@ -143,48 +208,69 @@ struct DecQ4K {
     m2 = (c < 2) ? 0u : 0x00300030u;
     shm = (c < 2) ? 0u : 4u;
   }
+  __device__ __forceinline__ void load_x_plain(const XStage& X, int sbcol, int c_, bool active) {
+    load(X, 256 * sbcol + 64 * c_, 256 * sbcol + 64 * c_ + 32, active);
+    xs0 = static_cast<float>(xsi[0] + xsi[1]);
+    xs1 = static_cast<float>(xsi[2] + xsi[3]);
+  }
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    load_x_plain(X, sbcol, c_, active);
+    xs1 *= 16.f;  // the high-nibble dot products come out 16 times too large: see row()
+    xf1 *= 0.0625f;
+  }
+  // d*s_lo, d*s_hi, dmin*m_lo, dmin*m_hi (times 2^-24) from the block header.
+  __device__ __forceinline__ void scales(const uint4 h, float& ds_lo, float& ds_hi, float& dm_lo, float& dm_hi) const {
+    const uint32_t s2 = (__byte_perm(h.y, h.w, sel_s) & m1) | ((__byte_perm(h.y, 0u, sel_h) >> 2) & m2);
+    const uint32_t m2v = ((__byte_perm(h.z, h.w, sel_s) >> shm) & m1) | ((__byte_perm(h.z, 0u, sel_h) >> 2) & m2);
+    mul1x2h(ds_lo, ds_hi, h.x, s2);
+    mul1x2h(dm_lo, dm_hi, h.x >> 16, m2v);
+  }
+  __device__ __forceinline__ float combine(int lo, int hi, float ds_lo, float ds_hi, float dm_lo, float dm_hi) const {
+    const float t0 = fmaf(ds_lo, static_cast<float>(lo), -dm_lo * xs0);
+    const float t1 = fmaf(ds_hi, static_cast<float>(hi), -dm_hi * xs1);
+    return fmaf(t0, xf0, t1 * xf1);
+  }
 
   __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
     const uint4 h = *reinterpret_cast<const uint4*>(blk);
     const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t wd = w[u], ws = wd >> 8;
-      fma2h(a0, a1, xr[4 * u + 0], wd & 0x000F000Fu);
-      fma2h(a2, a3, xr[4 * u + 1], ws & 0x000F000Fu);
-      fma2h(b0, b1, xr[4 * u + 2], wd & 0x00F000F0u);
-      fma2h(b2, b3, xr[4 * u + 3], ws & 0x00F000F0u);
+      // High nibbles stay in place: dp2a sees 16 q, and 16 * sum(x_i q) still fits int32
+      // (32 values * 240 * 2^15 < 2^28); the factor 16 is folded into xs1 and xf1.
+      const uint32_t L = w[u] & 0x0F0F0F0Fu, H = w[u] & 0xF0F0F0F0u;
+      int& al = (u & 1) ? a1 : a0;
+      int& ah = (u & 1) ? b1 : b0;
+      al = dp2a_lo_u(xr[2 * u], L, al);
+      al = dp2a_hi_u(xr[2 * u + 1], L, al);
+      ah = dp2a_lo_u(xr[16 + 2 * u], H, ah);
+      ah = dp2a_hi_u(xr[16 + 2 * u + 1], H, ah);
     }
-    const float acc_lo = (a0 + a1) + (a2 + a3);          // 2^-24 * sum x q (low nibbles)
-    const float acc_hi = ((b0 + b1) + (b2 + b3)) * 0.0625f;  // high nibbles sat 4 bits up
-    // scale and min pairs of groups 2c, 2c+1 spread into f16 halves
-    const uint32_t s2 = (__byte_perm(h.y, h.w, sel_s) & m1) | ((__byte_perm(h.y, 0u, sel_h) >> 2) & m2);
-    const uint32_t m2v = ((__byte_perm(h.z, h.w, sel_s) >> shm) & m1) | ((__byte_perm(h.z, 0u, sel_h) >> 2) & m2);
     float ds_lo, ds_hi, dm_lo, dm_hi;
-    mul1x2h(ds_lo, ds_hi, h.x, s2);          // d * s * 2^-24
-    mul1x2h(dm_lo, dm_hi, h.x >> 16, m2v);   // dmin * m * 2^-24
-    const float sq = fmaf(ds_lo, acc_lo, ds_hi * acc_hi);
-    const float mx = fmaf(dm_lo, xs[0], dm_hi * xs[1]);
-    return fmaf(sq, kTwo48, -mx);
+    scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
+    return combine(a0 + a1, b0 + b1, ds_lo, ds_hi, dm_lo, dm_hi);
   }
 };
 
 // ------------------------------------------------------------------------------- Q5_K
-// Q4_K's piece split and x order (quants at byte 48); the fifth bit of element 64c + t
-// (low) / 64c + 32 + t (high) is bit 2c / 2c+1 of qh[t] (qh at byte 16).  It is rotated
-// next to its nibble (bit 4 of a half for low nibbles, bit 8 for high nibbles, which
-// already sit 4 bits up) before the multiply.
+// Q4_K's piece split and activations (quants at byte 48); the fifth bit of element 64c + t
+// (low) / 64c + 32 + t (high) is bit 2c / 2c+1 of qh[t] (qh at byte 16).  A funnel shift
+// brings it to bit 4 of each byte, next to its nibble, before the dot product.
 struct DecQ5K : DecQ4K {
   static constexpr int kSB = 176, kSB2 = 0;
-  uint32_t rl, rh;  // rotate amounts bringing bit 2c to bit 4 and bit 2c+1 to bit 8
+  uint32_t rl, rh;  // rotate amounts bringing bit 2c / 2c+1 of each byte to bit 4
+
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    load_x_plain(X, sbcol, c_, active);
+  }
 
   __device__ __forceinline__ void init(int c_) {
     DecQ4K::init(c_);
     rl = (4u - 2u * c_) & 31u;
-    rh = (8u - 2u * c_ - 1u) & 31u;
+    rh = (3u - 2u * c_) & 31u;
   }
 
   __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
@@ -195,127 +281,108 @@ struct DecQ5K : DecQ4K {
     const uint4 qb = *reinterpret_cast<const uint4*>(blk + 64 + 32 * c);
     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t wd = w[u], ws = wd >> 8, ed = e[u], es = ed >> 8;
-      const uint32_t l02 = (wd & 0x000F000Fu) | (__funnelshift_l(ed, ed, rl) & 0x00100010u);
-      const uint32_t l13 = (ws & 0x000F000Fu) | (__funnelshift_l(es, es, rl) & 0x00100010u);
-      const uint32_t h02 = (wd & 0x00F000F0u) | (__funnelshift_l(ed, ed, rh) & 0x01000100u);
-      const uint32_t h13 = (ws & 0x00F000F0u) | (__funnelshift_l(es, es, rh) & 0x01000100u);
-      fma2h(a0, a1, xr[4 * u + 0], l02);
-      fma2h(a2, a3, xr[4 * u + 1], l13);
-      fma2h(b0, b1, xr[4 * u + 2], h02);
-      fma2h(b2, b3, xr[4 * u + 3], h13);
+      const uint32_t L = (w[u] & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rl) & 0x10101010u);
+      const uint32_t H = ((w[u] >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rh) & 0x10101010u);
+      int& al = (u & 1) ? a1 : a0;
+      int& ah = (u & 1) ? b1 : b0;
+      al = dp2a_lo_u(xr[2 * u], L, al);
+      al = dp2a_hi_u(xr[2 * u + 1], L, al);
+      ah = dp2a_lo_u(xr[16 + 2 * u], H, ah);
+      ah = dp2a_hi_u(xr[16 + 2 * u + 1], H, ah);
     }
-    const float acc_lo = (a0 + a1) + (a2 + a3);
-    const float acc_hi = ((b0 + b1) + (b2 + b3)) * 0.0625f;
-    const uint32_t s2 = (__byte_perm(h.y, h.w, sel_s) & m1) | ((__byte_perm(h.y, 0u, sel_h) >> 2) & m2);
-    const uint32_t m2v = ((__byte_perm(h.z, h.w, sel_s) >> shm) & m1) | ((__byte_perm(h.z, 0u, sel_h) >> 2) & m2);
     float ds_lo, ds_hi, dm_lo, dm_hi;
-    mul1x2h(ds_lo, ds_hi, h.x, s2);
-    mul1x2h(dm_lo, dm_hi, h.x >> 16, m2v);
-    const float sq = fmaf(ds_lo, acc_lo, ds_hi * acc_hi);
-    const float mx = fmaf(dm_lo, xs[0], dm_hi * xs[1]);
-    return fmaf(sq, kTwo48, -mx);
+    scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
+    return combine(a0 + a1, b0 + b1, ds_lo, ds_hi, dm_lo, dm_hi);
   }
 };
 
 // ------------------------------------------------------------------------------- Q6_K
 // Lane piece c: half H = c>>1, rr = c&1.  Byte ql[64H + 32rr + t] holds, in its low
 // nibble, element 128H + 32rr + t and, in its high nibble, element 128H + 32(rr+2) + t;
-// their top two bits are bits 2rr..2rr+1 / 2rr+4..2rr+5 of qh[32H + t].  The 6-bit
-// fields are assembled in the low bits of each half; the -32 offset is removed with the
-// activation sums of the four 16-element scale groups.  Blocks are 210 bytes (2-byte
+// their top two bits are bits 2rr..2rr+1 / 2rr+4..2rr+5 of qh[32H + t].  The 6-bit codes
+// are assembled bytewise and dotted with dp2a; the -32 offset is removed with the integer
+// sums of the activations of each 16-element scale group.  Blocks are 210 bytes (2-byte
 // aligned), so quant words are read as 16-bit pairs.
-struct DecQ6K {
+struct DecQ6K : IntX {
   static constexpr int kSB = 210, kSB2 = 0;
-  static constexpr bool kBf16X = false;
-  uint32_t xr[32];
-  float xs[4];  // 32 * 2^-24 * sums of groups (lo t<16, lo t>=16, hi t<16, hi t>=16)
   int c;
-  uint32_t s_lo, s_hi;  // shifts bringing qh bits 2rr / 2rr+4 to bit 4 of each byte
+  uint32_t rlo, rhi;  // rotate amounts bringing qh bits 2rr / 2rr+4 of each byte to bit 4
 
-  __device__ __forceinline__ static int run0(int c) { return 128 * (c >> 1) + 32 * (c & 1); }
-  __device__ __forceinline__ static int run1(int c) { return 128 * (c >> 1) + 32 * (c & 1) + 64; }
-  __device__ __forceinline__ static constexpr int xloc(int k, int h) { return DecQ4K::xloc(k, h); }
-  __device__ __forceinline__ static constexpr int xsum(int k, int) { return ((k & 3) < 2 ? 0 : 2) + ((k >> 2) >= 4 ? 1 : 0); }
-  __device__ __forceinline__ static float xsum_scale() { return 32.0f / kTwo24; }
-  __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t sb, int c_, bool active) {
-    load_x_f16(*this, x, sb, c_, active);
-  }
-
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
   __device__ __forceinline__ void init(int c_) {
     c = c_;
     const int rr = c & 1;
-    s_lo = 2 * rr;
-    s_hi = 2 * rr + 4;
+    rlo = (4u - 2u * rr) & 31u;
+    rhi = (32u - 2u * rr) & 31u;
+  }
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    const int k0 = 256 * sbcol + 128 * (c_ >> 1) + 32 * (c_ & 1);
+    load(X, k0, k0 + 64, active);
+    xsi[0] *= 32, xsi[1] *= 32, xsi[2] *= 32, xsi[3] *= 32;
+    xf0 *= 1.0f / kTwo24;
+    xf1 *= 1.0f / kTwo24;
   }
 
   __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
     const int H = c >> 1, rr = c & 1;
     const uint8_t* ql = blk + 64 * H + 32 * rr;
     const uint8_t* qh = blk + 128 + 32 * H;
-    float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    int acc[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t l = ld_u32_a2(ql + 4 * u), e = ld_u32_a2(qh + 4 * u);
-      const uint32_t lo6 = (l & 0x0F0F0F0Fu) | (((e >> s_lo) & 0x03030303u) << 4);
-      const uint32_t hi6 = ((l >> 4) & 0x0F0F0F0Fu) | (((e >> s_hi) & 0x03030303u) << 4);
+      const uint32_t lo6 = (l & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rlo) & 0x30303030u);
+      const uint32_t hi6 = ((l >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rhi) & 0x30303030u);
       const int g = u >> 2;
-      fma2h(acc[g][0], acc[g][1], xr[4 * u + 0], lo6 & 0x003F003Fu);
-      fma2h(acc[g][0], acc[g][1], xr[4 * u + 1], (lo6 >> 8) & 0x003F003Fu);
-      fma2h(acc[2 + g][0], acc[2 + g][1], xr[4 * u + 2], hi6 & 0x003F003Fu);
-      fma2h(acc[2 + g][0], acc[2 + g][1], xr[4 * u + 3], (hi6 >> 8) & 0x003F003Fu);
+      acc[g] = dp2a_lo_u(xr[2 * u], lo6, acc[g]);
+      acc[g] = dp2a_hi_u(xr[2 * u + 1], lo6, acc[g]);
+      acc[2 + g] = dp2a_lo_u(xr[16 + 2 * u], hi6, acc[2 + g]);
+      acc[2 + g] = dp2a_hi_u(xr[16 + 2 * u + 1], hi6, acc[2 + g]);
     }
     const int8_t* sc = reinterpret_cast<const int8_t*>(blk + 192 + 8 * H + 2 * rr);
     const float d = h2f(ld_u16(blk + 208));
-    float r = 0.f;
-    const int si[4] = {0, 1, 4, 5};
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      r = fmaf(static_cast<float>(sc[si[g]]), (acc[g][0] + acc[g][1]) - xs[g], r);
-    return d * r * kTwo24;
+    const float r0 = fmaf(static_cast<float>(sc[0]), static_cast<float>(acc[0] - xsi[0]),
+                          static_cast<float>(sc[1]) * static_cast<float>(acc[1] - xsi[1]));
+    const float r1 = fmaf(static_cast<float>(sc[4]), static_cast<float>(acc[2] - xsi[2]),
+                          static_cast<float>(sc[5]) * static_cast<float>(acc[3] - xsi[3]));
+    return d * fmaf(r0, xf0, r1 * xf1);
   }
 };
 
 // ------------------------------------------------------------------------------- Q8_0
-// A superblock is eight 34-byte blocks; lane piece c = blocks 2c and 2c+1.  Signed bytes
-// are biased to unsigned (q + 128) in the mask itself and the bias is removed with the
-// block's activation sum.  Register k of block e holds x pairs (t, t+2) / (t+1, t+3).
-struct DecQ80 {
+// A superblock is eight 34-byte blocks; lane piece c = blocks 2c and 2c+1 (elements
+// 64c + 32e + j).  The int8 codes are dotted directly with signed dp2a.
+struct DecQ80 : IntX {
   static constexpr int kSB = 272, kSB2 = 0;
-  static constexpr bool kBf16X = false;
-  uint32_t xr[32];
-  float xs[4];  // 128 * 2^-24 * sum of block 2c / 2c+1 activations
   int c;
 
-  __device__ __forceinline__ static int run0(int c) { return 64 * c; }
-  __device__ __forceinline__ static int run1(int c) { return 64 * c + 32; }
-  __device__ __forceinline__ static constexpr int xloc(int k, int h) { return 32 * (k >> 4) + 4 * ((k >> 1) & 7) + (k & 1) + 2 * h; }
-  __device__ __forceinline__ static constexpr int xsum(int k, int) { return k >> 4; }
-  __device__ __forceinline__ static float xsum_scale() { return 128.0f / kTwo24; }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
   __device__ __forceinline__ void init(int c_) { c = c_; }
-  __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t sb, int c_, bool active) {
-    load_x_f16(*this, x, sb, c_, active);
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    load(X, 256 * sbcol + 64 * c_, 256 * sbcol + 64 * c_ + 32, active);
+    xf0 *= 1.0f / kTwo24;
+    xf1 *= 1.0f / kTwo24;
   }
 
   __device__ __forceinline__ float row(const uint8_t* sblk, const uint8_t*) const {
-    float r = 0.f;
+    float r[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const uint8_t* blk = sblk + 34 * (2 * c + e);
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      int a0 = 0, a1 = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const uint32_t wd = ld_u32_a2(blk + 2 + 4 * u) ^ 0x80808080u;
-        fma2h(a0, a1, xr[16 * e + 2 * u], wd & 0x00FF00FFu);
-        fma2h(a2, a3, xr[16 * e + 2 * u + 1], (wd >> 8) & 0x00FF00FFu);
+        const uint32_t wd = ld_u32_a2(blk + 2 + 4 * u);
+        int& a = (u & 1) ? a1 : a0;
+        a = dp2a_lo_s(xr[16 * e + 2 * u], wd, a);
+        a = dp2a_hi_s(xr[16 * e + 2 * u + 1], wd, a);
       }
-      const float d = h2f(ld_u16(blk));
-      r = fmaf(d, ((a0 + a1) + (a2 + a3)) - xs[e], r);
+      r[e] = h2f(ld_u16(blk)) * static_cast<float>(a0 + a1);
     }
-    return r * kTwo24;
+    return fmaf(r[0], xf0, r[1] * xf1);
   }
 };
 
@@ -323,38 +390,45 @@ struct DecQ80 {
 // Superblock = 256 elements: 128 nibble bytes (stream 1) and 16 E4M3 scales (stream 2).
 // Lane piece c = nibble bytes [32c, 32c+32) and scales [4c, 4c+4); register k holds the
 // activations of nibble byte k (elements 2k, 2k+1: low nibble = even element).  E2M1 and
-// E4M3 are decoded by the hardware conversions to f16 (exact for every code).  The bf16
-// activations are staged as f16 times a power of two chosen per CTA from max |x|, so the
-// f16 x E2M1 products stay exact; the power of two is removed from the result.
+// E4M3 are decoded by the hardware conversions to f16 (exact for every code) and f16 x f16
+// products accumulate exactly in fp32.  The bf16 activations are staged per 32-element
+// chunk as f16 times a power of two chosen from the chunk's largest |x| so that every
+// value is below 2^14: f16 then holds each bf16 value exactly (values 2^27 times smaller
+// than the largest lose low bits); the power of two is removed per chunk from the result.
 struct DecNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
-  static constexpr bool kBf16X = true;
   uint32_t xr[32];
-  float xs[4];
+  float xf0, xf1;
   int c;
 
-  float inv_scale;  // the activations are held as f16(x * 2^e); partial sums are scaled back
-
-  __device__ __forceinline__ void init(int c_) { c = c_; }
-  // bf16 activations of the lane's 64 elements as f16 pairs, times one power of two chosen
-  // from their largest magnitude so that every value is below 2^14 and f16 holds it exactly
-  // (values 2^28 times smaller than the largest lose low bits).
-  __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t sb, int c_, bool active) {
-    uint32_t v[32];
-    load_runs(x, sb * 256 + 64 * c_, sb * 256 + 64 * c_ + 32, active, v);
-    float mx = 0.f;
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
+    const int e8 = static_cast<int>(chunk_max_mag(v) >> 7);  // bf16 biased exponent
+    // 2^(e8-127) <= max < 2^(e8-126): scale by 2^(140 - e8) to bring it below 2^14.
+    const float scale = p2(max(-126, min(126, 140 - e8)));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf2f(v[i])), fabsf(bf2f(v[i] >> 16))));
-    float scale = 1.0f;
-    if (mx > 0.f && mx < 3.0e38f) {
-      const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127 + 1;  // 2^(e-1) <= mx < 2^e
-      scale = p2(max(-126, min(127, 14 - e)));
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h2 = __floats2half2_rn(bf2f(w[k]) * scale, bf2f(w[k] >> 16) * scale);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    inv_scale = 1.0f / scale;
+    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((i & 3) == 0) X.e[i >> 2] = 1.0f / scale;
+  }
+  __device__ __forceinline__ void init(int c_) { c = c_; }
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    const int k0 = 256 * sbcol + 64 * c_;
+    if (active) {
+      uint32_t a[16], b[16];
+      ld_chunk(X.q + k0, a);
+      ld_chunk(X.q + k0 + 32, b);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const __half2 h2 = __floats2half2_rn(bf2f(v[k]) * scale, bf2f(v[k] >> 16) * scale);
-      xr[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
+      xf0 = X.e[k0 >> 5];
+      xf1 = X.e[(k0 >> 5) + 1];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xr[i] = 0u;
+      xf0 = xf1 = 0.f;
     }
   }
 
@@ -374,7 +448,7 @@ struct DecNVFP4 {
     const uint4 q1 = *reinterpret_cast<const uint4*>(nib + 32 * c + 16);
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     const uint32_t s4 = *reinterpret_cast<const uint32_t*>(sc + 4 * c) & 0x7F7F7F7Fu;  // |scale|
-    float r = 0.f;
+    float r[2] = {0.f, 0.f};
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -387,9 +461,9 @@ struct DecNVFP4 {
         fma2h(a2, a3, xr[8 * b + 4 * u + 3], e2m1x2(wd >> 24));
       }
       const float sv = h2f(e4m3x2((s4 >> (8 * b)) & 0xFFu));
-      r = fmaf(sv, (a0 + a1) + (a2 + a3), r);
+      r[b >> 1] = fmaf(sv, (a0 + a1) + (a2 + a3), r[b >> 1]);
     }
-    return r * inv_scale;
+    return fmaf(r[0], xf0, r[1] * xf1);
   }
 };
 
@@ -399,7 +473,8 @@ struct DecNVFP4 {
 // with F_k(b) = floor(3^k b / 256), g_k = y_{k-1} - 3 y_k, y_5 = 0; qh bytes carry four
 // digits, so their y_4 is 0 ("metal: TQ1_0 kernel performance", section 1).  F_k is one
 // round-toward-minus-infinity FMA: 2^23 + b * 3^k / 256 rounded down is 2^23 + F_k.  The
-// 65 coefficients g of a lane piece are staged in shared memory as fp32.
+// activations stay fp16 in the staging buffer; each lane keeps its 65 coefficients g in
+// registers as fp32.
 struct DecTQ10 {
   static constexpr int kSB = 54, kSB2 = 0;
   float g[13][5];
@@ -411,8 +486,11 @@ struct DecTQ10 {
     if (p < 48) return 160 + 16 * n + (p - 32);
     return 240 + 4 * n + (p - 48);
   }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
+    reinterpret_cast<uint4*>(X.q)[i] = v;
+  }
   __device__ __forceinline__ void init(int c_) { c = c_; }
-  __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t sb, int c_, bool active) {
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     xsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 13; ++i) {
@@ -421,7 +499,7 @@ struct DecTQ10 {
 #pragma unroll
       for (int n = 0; n < 5; ++n) {
         const bool has = active && !(p >= 48 && n == 4);
-        y[n] = has ? h2f(__ldg(x + sb * 256 + elem_of(p, n))) : 0.f;
+        y[n] = has ? h2f(X.q[256 * sbcol + elem_of(p, n)]) : 0.f;
         xsum += y[n];
       }
       y[5] = 0.f;

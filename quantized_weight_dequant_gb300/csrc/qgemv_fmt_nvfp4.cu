@@ -4,12 +4,6 @@
 
 namespace qg {
 
-const void* stream_kernel_nvfp4(int rows_per_item) {
-  switch (rows_per_item) {
-    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecNVFP4, 1>);
-    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecNVFP4, 2>);
-    default: return reinterpret_cast<const void*>(&stream_kernel<DecNVFP4, 4>);
-  }
-}
+const void* stream_kernel_nvfp4(int R, int D) { return stream_kernel_table<DecNVFP4>(R, D); }
 
 }  // namespace qg

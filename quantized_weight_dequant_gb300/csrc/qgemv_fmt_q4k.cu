@@ -4,12 +4,6 @@
 
 namespace qg {
 
-const void* stream_kernel_q4k(int rows_per_item) {
-  switch (rows_per_item) {
-    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecQ4K, 1>);
-    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecQ4K, 2>);
-    default: return reinterpret_cast<const void*>(&stream_kernel<DecQ4K, 4>);
-  }
-}
+const void* stream_kernel_q4k(int R, int D) { return stream_kernel_table<DecQ4K>(R, D); }
 
 }  // namespace qg

@@ -4,12 +4,6 @@
 
 namespace qg {
 
-const void* stream_kernel_q5k(int rows_per_item) {
-  switch (rows_per_item) {
-    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecQ5K, 1>);
-    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecQ5K, 2>);
-    default: return reinterpret_cast<const void*>(&stream_kernel<DecQ5K, 4>);
-  }
-}
+const void* stream_kernel_q5k(int R, int D) { return stream_kernel_table<DecQ5K>(R, D); }
 
 }  // namespace qg

@@ -4,12 +4,6 @@
 
 namespace qg {
 
-const void* stream_kernel_q6k(int rows_per_item) {
-  switch (rows_per_item) {
-    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecQ6K, 1>);
-    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecQ6K, 2>);
-    default: return reinterpret_cast<const void*>(&stream_kernel<DecQ6K, 4>);
-  }
-}
+const void* stream_kernel_q6k(int R, int D) { return stream_kernel_table<DecQ6K>(R, D); }
 
 }  // namespace qg

@@ -4,12 +4,6 @@
 
 namespace qg {
 
-const void* stream_kernel_tq10(int rows_per_item) {
-  switch (rows_per_item) {
-    case 1: return reinterpret_cast<const void*>(&stream_kernel<DecTQ10, 1>);
-    case 2: return reinterpret_cast<const void*>(&stream_kernel<DecTQ10, 2>);
-    default: return reinterpret_cast<const void*>(&stream_kernel<DecTQ10, 4>);
-  }
-}
+const void* stream_kernel_tq10(int R, int D) { return stream_kernel_table<DecTQ10>(R, D); }
 
 }  // namespace qg

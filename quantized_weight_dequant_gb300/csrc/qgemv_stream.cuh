@@ -5,15 +5,22 @@
 // 64-element piece in registers for the whole kernel, and the warp walks down the rows of
 // its row group, R rows per stage, streaming only its own slice of each row.
 //  * Weights reach shared memory through a private ring of D stages per warp, filled with
-//    16-byte cp.async copies (cache-global) issued by all 32 lanes.  A stage is consumed
-//    after cp.async.wait_group, which the hardware tracks per thread: a warp waiting for
-//    data stalls on its scoreboard and takes no issue slots from warps that are decoding.
-//  * Each lane decodes its piece of each row (qgemv_decode.cuh); the warp adds its 32
-//    lanes; the Wk partial sums of a row are added in a fixed order in shared memory at the
-//    end, so results are bitwise reproducible.
-//  * The first stages are requested before the programmatic-dependent-launch wait (they
-//    are weights, which the kernel this launch may overlap does not write); the
-//    activations are read after it.
+//    16-byte cp.async copies (cache-global): lane l copies bytes [16l + 512j, +16) of each
+//    row slice, with the base+offset address forms and the per-lane predicates computed
+//    once.  A stage is consumed after cp.async.wait_group, which the hardware tracks per
+//    thread: a warp waiting for data stalls on its scoreboard and takes no issue slots
+//    from warps that are decoding.
+//  * Each lane decodes its piece of each row of a stage (qgemv_decode.cuh).  The R row
+//    sums are reduced across the warp together: the first butterfly steps exchange whole
+//    rows, so 2 rows take 5 shuffles and 4 rows take 6 (instead of 5 per row).
+//    Rows past the end of the row group in its last stage are decoded from stale ring
+//    bytes and dropped; lanes past a short last K-column are zeroed.
+//  * The Wk partial sums of a row are added in a fixed order in shared memory at the end,
+//    so results are bitwise reproducible.
+//  * x is staged once per CTA in shared memory, converted there to the decoders' form
+//    (fixed point for the integer-code formats), then copied by each lane to registers.
+//  * Under programmatic dependent launch the first weight stages are requested before the
+//    wait for the previous kernel (weights are not written by it); x is read after it.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -21,6 +28,14 @@
 
 #include "qgemv_decode.cuh"
 #include "qgemv_ptx.cuh"
+
+// Optional tracing hooks for timeline studies: empty unless defined before this header.
+#ifndef QG_TRACE
+#define QG_TRACE(k)
+#endif
+#ifndef QG_TRACE_END
+#define QG_TRACE_END()
+#endif
 
 namespace qg {
 
@@ -32,15 +47,16 @@ struct StreamArgs {
   const uint16_t* x;    // activations (fp16, bf16 for NVFP4)
   float* y;
   int64_t N;
+  int rows_q, rows_rem; // N = gridDim.x * rows_q + rows_rem: CTA b has rows_q (+1 if b < rows_rem)
   int64_t row_bytes, row_bytes2;  // bytes per row of stream 1 / 2 (multiples of 16)
   int nsb;              // superblocks per row
   int Wk;               // K-columns (warps per row group) = ceil(nsb / 8)
   int P;                // row groups per CTA
-  int D;                // stages per warp: 2, 3, 4 or 6
   int red_rows;         // rows of the reduction buffer (>= rows of any CTA)
   int* err;
   uint64_t spin_ns;
   int test_stall;       // 1: warp 0 of CTA 0 also waits, bounded, on a barrier nothing completes
+  int pdl;              // launched with programmatic dependent launch
 };
 
 template <class Dec>
@@ -48,21 +64,34 @@ __host__ __device__ constexpr int slice_bytes() {
   return 8 * Dec::kSB + 8 * Dec::kSB2;
 }
 
-// Shared memory: [rings: warps * D * R * slice][reduction buffer][never-completing barrier]
-__host__ __device__ inline size_t stream_ring_bytes(int warps, int D, int R, int slice) {
-  return static_cast<size_t>(warps) * D * R * slice;
-}
-__host__ __device__ inline size_t stream_bar_offset(int warps, int D, int R, int slice, int Wk, int red_rows) {
-  size_t s = stream_ring_bytes(warps, D, R, slice);
-  if (Wk > 1) s += static_cast<size_t>(red_rows) * Wk * 4;
-  return (s + 15) & ~static_cast<size_t>(15);
-}
-__host__ __device__ inline size_t stream_smem_bytes(int warps, int D, int R, int slice, int Wk, int red_rows) {
-  return stream_bar_offset(warps, D, R, slice, Wk, red_rows) + 16;
+// Shared memory: [rings: warps * D * R * slice][reduction buffer][x staging: q (2K bytes),
+// e (K/32 floats), s (K/16 ints)][never-completing barrier], each part 16-byte aligned.
+struct StreamSmem {
+  size_t red, xq, xe, xs, bar, total;
+};
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
+__host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int slice, int Wk, int red_rows, int K) {
+  StreamSmem m;
+  m.red = static_cast<size_t>(warps) * D * R * slice;
+  m.xq = align16(m.red + (Wk > 1 ? static_cast<size_t>(red_rows) * Wk * 4 : 0));
+  m.xe = align16(m.xq + static_cast<size_t>(K) * 2);
+  m.xs = align16(m.xe + static_cast<size_t>(K / 32) * 4);
+  m.bar = align16(m.xs + static_cast<size_t>(K / 16) * 4);
+  m.total = m.bar + 16;
+  return m;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// cp_async16 at [dst + DOFF] <- [src + SOFF] when p != 0 (a predicated copy, no branch).
+template <int DOFF, int SOFF>
+__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void* src, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q cp.async.cg.shared.global [%0+%3], [%1+%4], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"(p), "n"(DOFF), "n"(SOFF)
+      : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -70,99 +99,58 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// One warp's whole life after set-up: prologue copies, activations, then the stage loop.
-template <class Dec, int R, int D>
-__device__ __forceinline__ void warp_stream(const StreamArgs& a, Dec& dec, uint8_t* ring, float* red, int64_t r_lo,
-                                            int64_t p_lo, int64_t nrows, int wk, int ncols, int lane) {
-  constexpr int SB = Dec::kSB, SB2 = Dec::kSB2, SLICE = slice_bytes<Dec>();
-  constexpr int STAGE = R * SLICE;
-  const int col = lane >> 2, c = lane & 3;
-  const bool active = col < ncols;
-  const int n1 = ncols * SB / 16, n2 = ncols * SB2 / 16;  // 16-byte copies per row
-  const int nst = static_cast<int>((nrows + R - 1) / R);
-  const uint32_t ring_s = smem_u32(ring);
-  const uint8_t* src1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB;
-  const uint8_t* src2 = (SB2 > 0) ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 : a.W;
-
-  auto issue = [&](int st) {
-    if (st < nst) {
-      const int r0 = st * R;
-      const int nr = static_cast<int>(min(static_cast<int64_t>(R), nrows - r0));
-      const uint32_t dst = ring_s + (st % D) * STAGE;
-      for (int r = 0; r < nr; ++r) {
-        const uint8_t* s1 = src1 + static_cast<int64_t>(r0 + r) * a.row_bytes;
-        for (int i = lane; i < n1; i += 32) cp_async16(dst + r * SLICE + 16 * i, s1 + 16 * i);
-        if (SB2 > 0) {
-          const uint8_t* s2 = src2 + static_cast<int64_t>(r0 + r) * a.row_bytes2;
-          for (int i = lane; i < n2; i += 32) cp_async16(dst + r * SLICE + 8 * SB + 16 * i, s2 + 16 * i);
-        }
-      }
-    }
-    cp_async_commit();
-  };
-
-#pragma unroll
-  for (int s = 0; s < D - 1; ++s) issue(s);
-  pdl_wait();
-  dec.load_x(a.x, 8 * wk + col, c, active);
-
-  for (int st = 0; st < nst; ++st) {
-    issue(st + D - 1);
-    cp_async_wait<D - 1>();
-    __syncwarp();
-    const uint8_t* s1 = ring + (st % D) * STAGE + col * SB;
-    const uint8_t* s2 = ring + (st % D) * STAGE + 8 * SB + col * SB2;
-    const int r0 = st * R;
-    const int nr = static_cast<int>(min(static_cast<int64_t>(R), nrows - r0));
-    float v[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] = 0.f;
-    if (active) {
-      if (nr == R) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = dec.row(s1 + r * SLICE, s2 + r * SLICE);
-      } else {  // last, partial stage of the row group
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (r < nr) v[r] = dec.row(s1 + r * SLICE, s2 + r * SLICE);
-      }
-    }
-    __syncwarp();  // every lane is done with this slot before it is refilled
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (r < nr) {
-        const float sum = warp_sum(v[r]);
-        if (lane == 0) {
-          const int64_t row = p_lo + r0 + r;
-          if (a.Wk == 1)
-            a.y[row] = sum;
-          else
-            red[(row - r_lo) * a.Wk + wk] = sum;
-        }
-      }
-    }
+// Sum of v[0..R) over the warp; lane l ends up holding the total of row l / (32 / R).
+template <int R>
+__device__ __forceinline__ float reduce_rows(const float (&v)[R], int lane) {
+  float t;
+  if constexpr (R == 1) {
+    t = v[0];
+  } else if constexpr (R == 2) {
+    const bool up = lane & 16;
+    t = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, up ? v[0] : v[1], 16);
+  } else {
+    static_assert(R == 4, "rows per stage: 1, 2 or 4");
+    const bool up = lane & 16;
+    const float k0 = (up ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, up ? v[0] : v[2], 16);
+    const float k1 = (up ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, up ? v[1] : v[3], 16);
+    const bool up8 = lane & 8;
+    t = (up8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8);
   }
-  cp_async_wait<0>();
+#pragma unroll
+  for (int o = 32 / R / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
 }
 
-template <class Dec, int R>
+template <class Dec, int R, int D>
 __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
+  QG_TRACE(0);
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int SLICE = slice_bytes<Dec>();
+  constexpr int SB = Dec::kSB, SB2 = Dec::kSB2, SLICE = slice_bytes<Dec>();
+  constexpr int STAGE = R * SLICE;
+  constexpr int J1 = (8 * SB / 16 + 31) / 32, J2 = (8 * SB2 / 16 + 31) / 32;  // copies per lane per row
+  constexpr int LPR = 32 / R;  // lanes per row after the reduction
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int p = warp / a.Wk, wk = warp % a.Wk;
 
-  const int64_t G = gridDim.x;
-  const int64_t r_lo = static_cast<int64_t>(blockIdx.x) * a.N / G;
-  const int64_t r_hi = (static_cast<int64_t>(blockIdx.x) + 1) * a.N / G;
-  const int64_t ncta = r_hi - r_lo;
-  const int64_t p_lo = r_lo + ncta * p / a.P, p_hi = r_lo + ncta * (p + 1) / a.P;
+  // Contiguous row ranges: CTA b, then row group p within it (no 64-bit division).
+  const int b = blockIdx.x;
+  const int64_t r_lo = static_cast<int64_t>(b) * a.rows_q + min(b, a.rows_rem);
+  const int ncta = a.rows_q + (b < a.rows_rem ? 1 : 0);
+  const int pq = ncta / a.P, prem = ncta % a.P;
+  const int64_t p_lo = r_lo + p * pq + min(p, prem);
+  const int nrows = pq + (p < prem ? 1 : 0);
   const int ncols = min(8, a.nsb - 8 * wk);
+  const int col = lane >> 2;
+  const bool active = col < ncols;
 
-  uint8_t* ring = smem + static_cast<size_t>(warp) * a.D * R * SLICE;
-  float* red = reinterpret_cast<float*>(smem + stream_ring_bytes(nwarps, a.D, R, SLICE));
-  uint64_t* never_bar = reinterpret_cast<uint64_t*>(smem + stream_bar_offset(nwarps, a.D, R, SLICE, a.Wk, a.red_rows));
+  const int K = 256 * a.nsb;
+  const StreamSmem L = stream_smem(nwarps, D, R, SLICE, a.Wk, a.red_rows, K);
+  uint8_t* ring = smem + static_cast<size_t>(warp) * D * STAGE;
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  const XStage X{reinterpret_cast<uint16_t*>(smem + L.xq), reinterpret_cast<float*>(smem + L.xe),
+                 reinterpret_cast<int*>(smem + L.xs)};
+  uint64_t* never_bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
   pdl_launch_dependents();  // the next kernel may start copying its weights right away
   if (a.test_stall && blockIdx.x == 0 && warp == 0) {
@@ -173,23 +161,141 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     }
     __syncwarp();
   }
+
+  // Copy set-up: lane chunk j of a row slice is bytes [16 * lane + 512 * j, +16).
+  const int n1 = ncols * SB / 16, n2 = ncols * SB2 / 16;
+  uint32_t ok1[J1], ok2[J2 > 0 ? J2 : 1];
+#pragma unroll
+  for (int j = 0; j < J1; ++j) ok1[j] = lane + 32 * j < n1;
+#pragma unroll
+  for (int j = 0; j < J2; ++j) ok2[j] = lane + 32 * j < n2;
+  const uint8_t* src1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
+  const uint8_t* src2 = (SB2 > 0) ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane : a.W;
+  const uint32_t dst0 = smem_u32(ring) + 16 * lane;
+  const int nst = (nrows + R - 1) / R;
+
+  // Requests stage st into ring slot `slot`: rows st * R + r of the row group, clamped to
+  // the last row (a short last stage re-reads that row into its spare slots; those rows
+  // are decoded and dropped), so no copy needs a row test.
+  auto issue = [&](int st, int slot) {
+    if (st < nst) {
+      const uint32_t dst = dst0 + slot * STAGE;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t row = min(st * R + r, nrows - 1);
+        const uint8_t* s1 = src1 + row * a.row_bytes;
+        const uint32_t d = dst + r * SLICE;
+#pragma unroll
+        for (int j = 0; j < J1; ++j) {
+          switch (j) {  // immediate offsets: 512 j
+            case 0: cp_async16_if<0, 0>(d, s1, ok1[j]); break;
+            case 1: cp_async16_if<512, 512>(d, s1, ok1[j]); break;
+            case 2: cp_async16_if<1024, 1024>(d, s1, ok1[j]); break;
+            case 3: cp_async16_if<1536, 1536>(d, s1, ok1[j]); break;
+            case 4: cp_async16_if<2048, 2048>(d, s1, ok1[j]); break;
+          }
+        }
+        if (SB2 > 0) {
+          const uint8_t* s2 = src2 + row * a.row_bytes2;
+#pragma unroll
+          for (int j = 0; j < J2; ++j) cp_async16_if<8 * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  static_assert(J1 <= 5, "row slice of at most 160 16-byte chunks");
+
+  // Activations: thread t copies 16-byte pieces t, t + blockDim.x, ... of x to the staging
+  // buffer (coalesced), then converts the same pieces in place, so only its own copies need
+  // to have landed.  Without programmatic dependent launch the x copies are requested
+  // first, ahead of the weight stages, so they are not queued behind them.  With it, the
+  // weight stages are requested before the wait for the previous kernel (whose output x
+  // may be), and x after.  The piece count K / 8 is a multiple of 32, so every warp runs
+  // the same number of conversions (they shuffle within groups of four lanes).  These
+  // loops run once per launch and are kept rolled: straight-line start-up code is fetched
+  // while the weight stream already loads the memory system.
+  const int npieces = K / 8;
+  auto issue_x = [&]() {
+#pragma unroll 1
+    for (int i = threadIdx.x; i < npieces; i += blockDim.x)
+      cp_async16(smem_u32(X.q) + 16 * i, reinterpret_cast<const uint4*>(a.x) + i);
+    cp_async_commit();
+  };
+  if (a.pdl) {
+#pragma unroll 1
+    for (int s = 0; s < D - 1; ++s) issue(s, s);
+    pdl_wait();
+    issue_x();
+    cp_async_wait<0>();
+  } else {
+    pdl_wait();  // returns at once: this launch does not overlap the previous kernel
+    issue_x();
+#pragma unroll 1
+    for (int s = 0; s < D - 1; ++s) issue(s, s);
+    cp_async_wait<D - 1>();
+  }
+  QG_TRACE(1);
+#pragma unroll 1
+  for (int i = threadIdx.x; i < npieces; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
+  __syncthreads();
+  QG_TRACE(2);
   Dec dec;
   dec.init(lane & 3);
-  const int64_t nrows = p_hi - p_lo;
-  switch (a.D) {
-    case 2: warp_stream<Dec, R, 2>(a, dec, ring, red, r_lo, p_lo, nrows, wk, ncols, lane); break;
-    case 3: warp_stream<Dec, R, 3>(a, dec, ring, red, r_lo, p_lo, nrows, wk, ncols, lane); break;
-    case 4: warp_stream<Dec, R, 4>(a, dec, ring, red, r_lo, p_lo, nrows, wk, ncols, lane); break;
-    default: warp_stream<Dec, R, 6>(a, dec, ring, red, r_lo, p_lo, nrows, wk, ncols, lane); break;
+  dec.load_x(X, 8 * wk + col, lane & 3, active);
+
+  int slot = 0;  // ring slot of stage st; stage st + D - 1 goes to the slot freed by st - 1
+  for (int st = 0; st < nst; ++st) {
+    issue(st + D - 1, slot == 0 ? D - 1 : slot - 1);
+    cp_async_wait<D - 1>();
+    __syncwarp();
+    if (st == 0) QG_TRACE(3);
+    const uint8_t* s1 = ring + slot * STAGE + col * SB;
+    const uint8_t* s2 = ring + slot * STAGE + 8 * SB + col * SB2;
+    float v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] = dec.row(s1 + r * SLICE, s2 + r * SLICE);
+    __syncwarp();  // every lane is done with this slot before it is refilled
+    slot = (slot == D - 1) ? 0 : slot + 1;
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] = active ? v[r] : 0.f;
+    const float sum = reduce_rows<R>(v, lane);
+    const int row = st * R + lane / LPR;
+    if (lane % LPR == 0 && row < nrows) {
+      if (a.Wk == 1)
+        a.y[p_lo + row] = sum;
+      else
+        red[(p_lo - r_lo + row) * a.Wk + wk] = sum;
+    }
   }
+  cp_async_wait<0>();
+  QG_TRACE(4);
+
   if (a.Wk > 1) {
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < ncta; i += blockDim.x) {
+    for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
       float s = 0.f;
       for (int w = 0; w < a.Wk; ++w) s += red[i * a.Wk + w];
       a.y[r_lo + i] = s;
     }
   }
+  QG_TRACE(5);
+  QG_TRACE_END();
+}
+
+// Kernel table of one decoder: R in {1, 2, 4} rows per stage, D in {2, 3, 4} ring stages.
+template <class Dec>
+const void* stream_kernel_table(int R, int D) {
+  const int ri = R >= 4 ? 2 : R >= 2 ? 1 : 0;
+  const int di = D >= 4 ? 2 : D >= 3 ? 1 : 0;
+  static const void* const t[3][3] = {
+      {reinterpret_cast<const void*>(&stream_kernel<Dec, 1, 2>), reinterpret_cast<const void*>(&stream_kernel<Dec, 1, 3>),
+       reinterpret_cast<const void*>(&stream_kernel<Dec, 1, 4>)},
+      {reinterpret_cast<const void*>(&stream_kernel<Dec, 2, 2>), reinterpret_cast<const void*>(&stream_kernel<Dec, 2, 3>),
+       reinterpret_cast<const void*>(&stream_kernel<Dec, 2, 4>)},
+      {reinterpret_cast<const void*>(&stream_kernel<Dec, 4, 2>), reinterpret_cast<const void*>(&stream_kernel<Dec, 4, 3>),
+       reinterpret_cast<const void*>(&stream_kernel<Dec, 4, 4>)}};
+  return t[ri][di];
 }
 
 }  // namespace qg
