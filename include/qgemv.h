@@ -72,8 +72,11 @@ typedef enum {
 typedef struct qgemv_handle_s* qgemv_handle_t;
 
 /* Create a handle on CUDA device `device` (made current for the call).  Queries the SM
- * count and L2 size and allocates the handle's only device memory, a 4-byte error word.  *h receives the handle.  Returns QGEMV_ERR_NO_DEVICE
- * when the device is missing or is not compute capability 10.3. */
+ * count and L2 size and allocates the handle's device memory: a 4-byte error word, a 16 MiB
+ * workspace for split-K column sums and 4 KiB of per-range counters (zeroed here; every
+ * launch leaves them at zero).  *h receives the handle.  Returns QGEMV_ERR_NO_DEVICE when
+ * the device is missing or is not compute capability 10.3, QGEMV_ERR_OOM when an allocation
+ * fails. */
 qgemv_status_t qgemv_create(qgemv_handle_t* h, int device);
 
 /* Free the handle's device memory and the handle.  Waits for nothing: the caller must
@@ -86,8 +89,11 @@ qgemv_status_t qgemv_destroy(qgemv_handle_t h);
  *   y        device, N fp32 values, 16-byte aligned; must not overlap x or packed_W.
  *   N >= 1; K >= 1 and a multiple of 256 (Q4_K, Q5_K, Q6_K, TQ1_0), 32 (Q8_0) or 16 (NVFP4).
  * The call is asynchronous on `stream` (0 = legacy default stream), allocates nothing and
- * does not synchronise.  Results are deterministic: the same inputs and shape give
- * bitwise-identical y on every call (fixed reduction order, no atomics). */
+ * does not synchronise.  It may use the handle's workspace, so calls on one handle must not
+ * run at the same time on the GPU: calls ordered on one stream are fine; concurrent streams
+ * need one handle each.  Results are deterministic: the same inputs and shape give
+ * bitwise-identical y on every call (every sum is taken in a fixed order; the one atomic,
+ * a per-range arrival count, only picks which CTA adds the column sums). */
 qgemv_status_t qgemv_run(qgemv_handle_t h, qgemv_format_t fmt, const void* x, const void* packed_W,
                          int64_t N, int64_t K, float* y, cudaStream_t stream);
 
@@ -146,7 +152,13 @@ int qgemv_group_size(qgemv_format_t fmt);
  *   QGEMV_OPT_CTAS_PER_SM     streaming kernel CTAs per SM, 1 or 2 (default 2, used when
  *                             a row needs at most 8 warps); with 1, each CTA takes about half
  *                             an SM, so the next kernel of a programmatic-dependent-launch
- *                             chain can start on the other half. */
+ *                             chain can start on the other half.
+ *   QGEMV_OPT_KSPLIT          0 (default): when K > 4096 and N * ceil(K / 2048) <= 4 Mi, each
+ *                             CTA of the streaming kernel takes one 2048-wide K-column of a
+ *                             range of rows (so it reads only that part of x) and the column
+ *                             sums of a row meet in the handle's workspace, where the last
+ *                             CTA of the range adds them in column order.  1: each CTA covers
+ *                             every K-column of its rows and adds them in shared memory. */
 typedef enum {
   QGEMV_OPT_FORCE_PATH = 0,
   QGEMV_OPT_RING_DEPTH = 2,
@@ -154,7 +166,8 @@ typedef enum {
   QGEMV_OPT_SPIN_LIMIT_NS = 4,
   QGEMV_OPT_PDL = 5,
   QGEMV_OPT_TEST_STALL = 6,
-  QGEMV_OPT_CTAS_PER_SM = 7
+  QGEMV_OPT_CTAS_PER_SM = 7,
+  QGEMV_OPT_KSPLIT = 8
 } qgemv_option_t;
 
 qgemv_status_t qgemv_set_option(qgemv_handle_t h, qgemv_option_t opt, int64_t value);

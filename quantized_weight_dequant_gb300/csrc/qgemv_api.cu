@@ -20,6 +20,8 @@ using namespace qg;
 
 constexpr int kMaxWarps = 16;                    // per CTA (launch bound 512 threads)
 constexpr size_t kRedBudget = 16 * 1024;         // cross-warp reduction buffer per CTA
+constexpr size_t kWsFloats = size_t{4} << 20;    // split-K column sums: N * K-columns <= 4 Mi
+constexpr int kMaxRanges = 1024;                 // split-K row ranges (one counter each)
 
 struct Handle {
   int device = 0;
@@ -27,7 +29,10 @@ struct Handle {
   int l2_bytes = 0;
   size_t smem_optin = 0;
   int* err = nullptr;
+  float* ws = nullptr;  // split-K column sums
+  int* cnt = nullptr;   // split-K per-range arrival counts, zero between launches
   int ctas_per_sm = 2;
+  int ksplit = 0;       // 0: split K-columns over CTAs when the workspace holds them; 1: never
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   int force_path = 0;
   int ring_depth = 0;
@@ -136,22 +141,38 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   }
   const int Wk = static_cast<int>(Wk64);
   const int cps = (Wk <= kMaxWarps / 2) ? h.ctas_per_sm : 1;  // CTAs per SM
-  const int P = std::max(1, (kMaxWarps / cps) / Wk);
-  const int warps = P * Wk;
-  int64_t grid = std::min<int64_t>(int64_t{h.sms} * cps, (N + P - 1) / P);
-  if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
-  grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
-  if (N / grid >= 0x7ffffffe) {  // per-CTA row counts are 32-bit in the kernel
+  // Split mode: a CTA takes one K-column of a row range with all its warps, so it stages only
+  // that column of x; column sums meet in the workspace.  Fused mode: a CTA covers all
+  // K-columns of its rows and adds the column sums in shared memory.
+  // Two columns are faster fused (their x is small); from three on the split pays.
+  const bool split = Wk == 1 || (h.ksplit == 0 && Wk >= 3 && static_cast<double>(N) * Wk <= static_cast<double>(kWsFloats));
+  const int P = split ? kMaxWarps / cps : std::max(1, (kMaxWarps / cps) / Wk);
+  const int warps = split ? P : P * Wk;
+  int64_t ranges, grid;
+  if (split) {
+    ranges = std::min<int64_t>(std::max(1, (h.sms * cps) / Wk), (N + P - 1) / P);
+    ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));
+    grid = ranges * Wk;
+  } else {
+    grid = std::min<int64_t>(int64_t{h.sms} * cps, (N + P - 1) / P);
+    if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
+    grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
+    ranges = grid;
+  }
+  if (N / ranges >= 0x7ffffffe) {  // per-CTA row counts are 32-bit in the kernel
     rowwarp_plan(h, N, pl);
     return QGEMV_OK;
   }
-  const int red_rows = static_cast<int>((N + grid - 1) / grid + 1);
+  const int red_rows = split ? 0 : static_cast<int>((N + grid - 1) / grid + 1);
+  const int Kx = split ? static_cast<int>(std::min<int64_t>(K, 2048)) : static_cast<int>(K);
   const int slice = slice_of(f);
-  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : 2;
-  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : 4;
+  // Defaults: 2 rows per stage, 4 stages; split launches (long K): 4 rows, 2 stages.
+  const bool long_k = split && Wk > 1;
+  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : (long_k ? 4 : 2);
+  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : (long_k ? 2 : 4);
   const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
   auto limit = [&](int d, int r) { return std::min(h.dyn_smem_max[f][r_index(r)][d_index(d)], cap); };
-  auto smem_of = [&](int d, int r) { return stream_smem(warps, d, r, slice, Wk, red_rows, static_cast<int>(K)).total; };
+  auto smem_of = [&](int d, int r) { return stream_smem(warps, d, r, slice, Wk, red_rows, Kx).total; };
   while (smem_of(D, R) > limit(D, R) && (D > 2 || R > 1)) {
     if (D > 2)
       --D;
@@ -165,8 +186,8 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   }
   StreamArgs& a = pl.sa;
   a.N = N;
-  a.rows_q = static_cast<int>(N / grid);
-  a.rows_rem = static_cast<int>(N % grid);
+  a.rows_q = static_cast<int>(N / ranges);
+  a.rows_rem = static_cast<int>(N % ranges);
   a.row_bytes = rb1;
   a.row_bytes2 = rb2;
   a.nsb = static_cast<int>(nsb);
@@ -177,6 +198,9 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   a.spin_ns = h.spin_ns;
   a.test_stall = h.test_stall;
   a.pdl = h.pdl;
+  a.split = split ? 1 : 0;
+  a.ws = h.ws;
+  a.cnt = h.cnt;
   pl.path = 1;
   pl.grid = static_cast<int>(grid);
   pl.threads = 32 * warps;
@@ -268,13 +292,17 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
   auto release = [h]() {
     cudaGetLastError();
     cudaFree(h->err);
+    cudaFree(h->ws);
+    cudaFree(h->cnt);
     delete h;
   };
-  if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) {
+  if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess || cudaMalloc(&h->ws, kWsFloats * sizeof(float)) != cudaSuccess ||
+      cudaMalloc(&h->cnt, kMaxRanges * sizeof(int)) != cudaSuccess) {
     release();
     return QGEMV_ERR_OOM;
   }
-  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess || cudaMemset(h->cnt, 0, kMaxRanges * sizeof(int)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     release();
     return QGEMV_ERR_CUDA;
   }
@@ -302,6 +330,8 @@ qgemv_status_t qgemv_destroy(qgemv_handle_t hh) {
   Handle* h = reinterpret_cast<Handle*>(hh);
   if (!h) return QGEMV_OK;
   cudaFree(h->err);
+  cudaFree(h->ws);
+  cudaFree(h->cnt);
   delete h;
   return QGEMV_OK;
 }
@@ -338,6 +368,10 @@ qgemv_status_t qgemv_set_option(qgemv_handle_t hh, qgemv_option_t opt, int64_t v
       if (v < 1 || v > 2) return QGEMV_ERR_INVALID_ARG;
       h->ctas_per_sm = static_cast<int>(v);
       return QGEMV_OK;
+    case QGEMV_OPT_KSPLIT:
+      if (v < 0 || v > 1) return QGEMV_ERR_INVALID_ARG;
+      h->ksplit = static_cast<int>(v);
+      return QGEMV_OK;
   }
   return QGEMV_ERR_INVALID_ARG;
 }
@@ -352,8 +386,9 @@ qgemv_status_t qgemv_describe(qgemv_handle_t hh, qgemv_format_t fmt, int64_t N, 
   if (buf && len) {
     if (pl.path == 1)
       snprintf(buf, len,
-               "path=stream grid=%d block=%d kcols=%d row_groups=%d rows_per_stage=%d ring=%d smem=%zu pdl=%d",
-               pl.grid, pl.threads, pl.sa.Wk, pl.sa.P, pl.R, pl.D, pl.smem, h->pdl);
+               "path=stream grid=%d block=%d kcols=%d split=%d row_groups=%d rows_per_stage=%d ring=%d smem=%zu "
+               "pdl=%d",
+               pl.grid, pl.threads, pl.sa.Wk, pl.sa.split, pl.sa.P, pl.R, pl.D, pl.smem, h->pdl);
     else
       snprintf(buf, len, "path=rowwarp grid=%d block=%d", pl.rw_grid, pl.rw_block);
   }

@@ -57,6 +57,12 @@ struct StreamArgs {
   uint64_t spin_ns;
   int test_stall;       // 1: warp 0 of CTA 0 also waits, bounded, on a barrier nothing completes
   int pdl;              // launched with programmatic dependent launch
+  // Split mode (split = 1): CTA b takes K-column b % Wk of the rows of row range b / Wk, all
+  // its warps on that column (P = warps).  With Wk > 1 the column sums go to ws[kc * N + row]
+  // and the last CTA of a row range (counted in cnt[range], left at 0 again) adds them.
+  int split;
+  float* ws;
+  int* cnt;
 };
 
 template <class Dec>
@@ -131,10 +137,14 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   constexpr int LPR = 32 / R;  // lanes per row after the reduction
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int p = warp / a.Wk, wk = warp % a.Wk;
+  // Fused mode: warp = (row group p, K-column wk) over all Wk columns of the CTA's rows.
+  // Split mode: every warp of the CTA is on K-column blockIdx.x % Wk.
+  const int p = a.split ? warp : warp / a.Wk;
+  const int wk = a.split ? static_cast<int>(blockIdx.x % a.Wk) : warp % a.Wk;
+  const int kc0 = a.split ? wk : 0, kc1 = a.split ? wk + 1 : a.Wk;  // K-columns this CTA reads
 
-  // Contiguous row ranges: CTA b, then row group p within it (no 64-bit division).
-  const int b = blockIdx.x;
+  // Contiguous row ranges: range b, then row group p within it (no 64-bit division).
+  const int b = a.split ? static_cast<int>(blockIdx.x / a.Wk) : static_cast<int>(blockIdx.x);
   const int64_t r_lo = static_cast<int64_t>(b) * a.rows_q + min(b, a.rows_rem);
   const int ncta = a.rows_q + (b < a.rows_rem ? 1 : 0);
   const int pq = ncta / a.P, prem = ncta % a.P;
@@ -144,8 +154,9 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   const int col = lane >> 2;
   const bool active = col < ncols;
 
-  const int K = 256 * a.nsb;
-  const StreamSmem L = stream_smem(nwarps, D, R, SLICE, a.Wk, a.red_rows, K);
+  // The staging buffer holds the K-columns this CTA reads: all of x (fused) or one column.
+  const int Kx = a.split ? min(2048, 256 * a.nsb) : 256 * a.nsb;
+  const StreamSmem L = stream_smem(nwarps, D, R, SLICE, a.Wk, a.red_rows, Kx);
   uint8_t* ring = smem + static_cast<size_t>(warp) * D * STAGE;
   float* red = reinterpret_cast<float*>(smem + L.red);
   const XStage X{reinterpret_cast<uint16_t*>(smem + L.xq), reinterpret_cast<float*>(smem + L.xe),
@@ -215,11 +226,12 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   // the same number of conversions (they shuffle within groups of four lanes).  These
   // loops run once per launch and are kept rolled: straight-line start-up code is fetched
   // while the weight stream already loads the memory system.
-  const int npieces = K / 8;
+  // Pieces of the K-columns this CTA reads (32 per superblock, so whole warps drop out).
+  const int pc0 = 256 * kc0, pc1 = 32 * min(a.nsb, 8 * kc1);
   auto issue_x = [&]() {
 #pragma unroll 1
-    for (int i = threadIdx.x; i < npieces; i += blockDim.x)
-      cp_async16(smem_u32(X.q) + 16 * i, reinterpret_cast<const uint4*>(a.x) + i);
+    for (int i = pc0 + threadIdx.x; i < pc1; i += blockDim.x)
+      cp_async16(smem_u32(X.q) + 16 * (i - pc0), reinterpret_cast<const uint4*>(a.x) + i);
     cp_async_commit();
   };
   if (a.pdl) {
@@ -237,12 +249,12 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   }
   QG_TRACE(1);
 #pragma unroll 1
-  for (int i = threadIdx.x; i < npieces; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
+  for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
   __syncthreads();
   QG_TRACE(2);
   Dec dec;
   dec.init(lane & 3);
-  dec.load_x(X, 8 * wk + col, lane & 3, active);
+  dec.load_x(X, 8 * (wk - kc0) + col, lane & 3, active);  // superblock index within the buffer
 
   int slot = 0;  // ring slot of stage st; stage st + D - 1 goes to the slot freed by st - 1
   for (int st = 0; st < nst; ++st) {
@@ -264,6 +276,8 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     if (lane % LPR == 0 && row < nrows) {
       if (a.Wk == 1)
         a.y[p_lo + row] = sum;
+      else if (a.split)
+        a.ws[wk * a.N + p_lo + row] = sum;
       else
         red[(p_lo - r_lo + row) * a.Wk + wk] = sum;
     }
@@ -271,12 +285,35 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   cp_async_wait<0>();
   QG_TRACE(4);
 
-  if (a.Wk > 1) {
+  if (a.Wk > 1 && !a.split) {
     __syncthreads();
     for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
       float s = 0.f;
       for (int w = 0; w < a.Wk; ++w) s += red[i * a.Wk + w];
       a.y[r_lo + i] = s;
+    }
+  } else if (a.Wk > 1) {
+    // Publish this CTA's column sums, then count the CTA in; the last of the Wk CTAs of the
+    // row range adds the Wk column sums of each row in column order and resets the count.
+    __shared__ int last;
+    __syncthreads();  // every column sum of this CTA is written
+    if (threadIdx.x == 0) {
+      __threadfence();  // ... and visible device-wide (cumulative over the barrier) before the count
+      last = atomicAdd(a.cnt + b, 1) == a.Wk - 1;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
+        float v[16];  // all column sums of the row in flight at once (Wk <= 16)
+#pragma unroll
+        for (int w = 0; w < 16; ++w) v[w] = w < a.Wk ? __ldcg(a.ws + w * a.N + r_lo + i) : 0.f;
+        float s = v[0];
+#pragma unroll
+        for (int w = 1; w < 16; ++w) s += v[w];  // column order; the zero padding adds nothing
+        a.y[r_lo + i] = s;
+      }
+      if (threadIdx.x == 0) a.cnt[b] = 0;
     }
   }
   QG_TRACE(5);

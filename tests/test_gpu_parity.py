@@ -81,17 +81,24 @@ def test_plain_row_path_matches_oracle(h, fmt, N, K):
         qgemv.set_option(h, qgemv.OPT_FORCE_PATH, 0)
 
 
-@pytest.mark.parametrize("cps,pdl", [(1, 0), (1, 1), (2, 1)])
-@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.NVFP4, synth.Q6_K])
-def test_launch_variants_match_oracle(h, fmt, cps, pdl):
+@pytest.mark.parametrize("ksplit", [0, 1])
+@pytest.mark.parametrize("cps,pdl", [(2, 0), (1, 0), (1, 1), (2, 1)])
+@pytest.mark.parametrize("fmt", ALL)
+def test_launch_variants_match_oracle(h, fmt, cps, pdl, ksplit):
+    """CTAs per SM, programmatic dependent launch, and split-K (one K-column per CTA, column
+    sums added by the last CTA of each row range) against K-columns added in the CTA."""
     qgemv.set_option(h, qgemv.OPT_CTAS_PER_SM, cps)
     qgemv.set_option(h, qgemv.OPT_PDL, pdl)
+    qgemv.set_option(h, qgemv.OPT_KSPLIT, ksplit)
     try:
-        _check_full(h, fmt, 70, 14336, seed=11 * cps + pdl + fmt, what=f"cps={cps} pdl={pdl}")
-        _check_full(h, fmt, 333, 4096, seed=13 * cps + pdl + fmt, what=f"cps={cps} pdl={pdl}")
+        for N, K in [(70, 14336), (333, 4096), (5, 12288), (1, 32768), (600, 2304)]:
+            d = qgemv.describe(h, fmt, N, K)
+            assert "rowwarp" in d or f"split={int((ksplit == 0 and K > 4096) or K <= 2048)}" in d, d
+            _check_full(h, fmt, N, K, seed=11 * cps + pdl + fmt + N, what=f"cps={cps} pdl={pdl} ksplit={ksplit}")
     finally:
         qgemv.set_option(h, qgemv.OPT_CTAS_PER_SM, 2)
         qgemv.set_option(h, qgemv.OPT_PDL, 0)
+        qgemv.set_option(h, qgemv.OPT_KSPLIT, 0)
 
 
 @pytest.mark.parametrize("depth,rows", [(2, 1), (3, 3), (8, 2), (4, 8)])
