@@ -66,7 +66,8 @@ typedef enum {
   QGEMV_ERR_CUDA = 5,               /* a CUDA runtime call or kernel launch failed */
   QGEMV_ERR_TIMEOUT = 6,            /* a kernel gave up on a bounded wait (see check_error) */
   QGEMV_ERR_OOM = 7,                /* qgemv_create could not allocate its workspace */
-  QGEMV_ERR_NO_DEVICE = 8           /* no usable CUDA device / not an sm_103 device */
+  QGEMV_ERR_NO_DEVICE = 8,          /* no usable CUDA device / not an sm_103 device */
+  QGEMV_ERR_TOO_LARGE = 9           /* shape needs more than qgemv_run_noalloc's fixed scratch */
 } qgemv_status_t;
 
 typedef struct qgemv_handle_s* qgemv_handle_t;
@@ -180,6 +181,40 @@ qgemv_status_t qgemv_describe(qgemv_handle_t h, qgemv_format_t fmt, int64_t N, i
 
 /* Compile-time build marker, checked by the Python binding at load (provenance). */
 const char* qgemv_build_marker(void);
+
+/* Capacity of qgemv_run_noalloc's scratch, in fp32 column sums: N * ceil(K / 2048) of them. */
+#define QGEMV_NOALLOC_MAX_COLUMN_SUMS 262144
+
+/* qgemv_run without a handle and without allocating anything.  (This entry point is part
+ * of the library's interface only; the pages that describe the method have no
+ * counterpart.)  It exists for callers that may not call cudaMalloc: code that runs under
+ * a host application owning all device memory (a plug-in given fixed buffers), processes
+ * whose allocator is capped or instrumented so a new allocation would fail or be refused,
+ * and latency-critical paths where an allocation's implicit synchronisation is not
+ * acceptable.  Those callers cannot use qgemv_create, which allocates the handle's
+ * workspace.
+ *
+ * Computes y = x . dequant(W)^T exactly like qgemv_run with the split-K streaming kernel:
+ * every CTA takes one 2048-wide K-column of a range of rows, and the column sums of a row
+ * are added in column order.  Arguments, layouts and results are those of qgemv_run;
+ * results are bitwise reproducible from call to call.  Shapes: K a multiple of 256 and at
+ * most 32768, with packed rows a multiple of 16 bytes (K a multiple of 2048 for Q6_K and
+ * TQ1_0), else QGEMV_ERR_BAD_SHAPE.  When K > 2048, N * ceil(K / 2048) must not exceed
+ * QGEMV_NOALLOC_MAX_COLUMN_SUMS, else QGEMV_ERR_TOO_LARGE and nothing is launched.
+ *
+ * Scratch: fixed arrays in the library's device memory (1 MiB of column sums, 4 KiB of
+ * counters), which every GPU that loads the library holds until the process exits.  All
+ * calls on a device share them and they keep what the last call left: each call first
+ * clears the counters with cudaMemsetAsync on `stream`, then launches.  Calls that may run
+ * at the same time on the GPU (different streams, or host threads that do not order their
+ * streams) race on the scratch and give wrong results; order them on one stream.
+ *
+ * The first call on a device (the current device) sets that device up: it looks up the
+ * scratch arrays' device addresses with cudaGetSymbolAddress and sets the kernels'
+ * shared-memory attribute.  Make that first call before any stream capture begins.
+ * Asynchronous on `stream`; does not synchronise. */
+qgemv_status_t qgemv_run_noalloc(qgemv_format_t fmt, const void* x, const void* packed_W, int64_t N, int64_t K,
+                                 float* y, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

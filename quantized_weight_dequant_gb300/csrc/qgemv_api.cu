@@ -263,6 +263,7 @@ const char* qgemv_status_string(qgemv_status_t s) {
     case QGEMV_ERR_TIMEOUT: return "kernel wait timed out";
     case QGEMV_ERR_OOM: return "out of device memory";
     case QGEMV_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case QGEMV_ERR_TOO_LARGE: return "shape exceeds the fixed scratch of qgemv_run_noalloc";
   }
   return "unknown status";
 }

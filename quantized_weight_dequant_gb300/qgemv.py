@@ -16,13 +16,14 @@ OPT_FORCE_PATH, OPT_RING_DEPTH, OPT_ROWS_PER_STAGE, OPT_SPIN_LIMIT_NS, OPT_PDL, 
     OPT_KSPLIT = 0, 2, 3, 4, 5, 6, 7, 8
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED_FORMAT", 3: "QGEMV_ERR_BAD_SHAPE",
           4: "QGEMV_ERR_MISALIGNED", 5: "QGEMV_ERR_CUDA", 6: "QGEMV_ERR_TIMEOUT", 7: "QGEMV_ERR_OOM",
-          8: "QGEMV_ERR_NO_DEVICE"}
+          8: "QGEMV_ERR_NO_DEVICE", 9: "QGEMV_ERR_TOO_LARGE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_FORMAT, ERR_BAD_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
-    ERR_NO_DEVICE = range(9)
+    ERR_NO_DEVICE, ERR_TOO_LARGE = range(10)
+NOALLOC_MAX_COLUMN_SUMS = 262144  # QGEMV_NOALLOC_MAX_COLUMN_SUMS
 
 EXPORTS = ["qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
            "qgemv_status_string", "qgemv_packed_bytes", "qgemv_group_size", "qgemv_set_option",
-           "qgemv_describe", "qgemv_build_marker"]
+           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc"]
 
 _lib = None
 
@@ -54,8 +55,9 @@ def lib() -> ctypes.CDLL:
         L.qgemv_set_option.argtypes = [vp, ctypes.c_int, i64]
         L.qgemv_describe.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_char_p, ctypes.c_size_t]
         L.qgemv_build_marker.restype = ctypes.c_char_p
+        L.qgemv_run_noalloc.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp, vp]
         for name in ("qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
-                     "qgemv_set_option", "qgemv_describe"):
+                     "qgemv_set_option", "qgemv_describe", "qgemv_run_noalloc"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -137,6 +139,15 @@ def run(h: Handle, fmt: int, x, packed_W, N: int, K: int, y, stream=None, check:
     st = lib().qgemv_run(h.ptr, fmt, _ptr(x), _ptr(packed_W), N, K, _ptr(y), _stream(stream))
     if check:
         _check(st, "qgemv_run")
+    return st
+
+
+def run_noalloc(fmt: int, x, packed_W, N: int, K: int, y, stream=None, check: bool = True) -> int:
+    """qgemv_run_noalloc: the same GEMV without a handle, using the library's fixed scratch
+    (for callers that may not allocate device memory).  Calls must not overlap on the GPU."""
+    st = lib().qgemv_run_noalloc(fmt, _ptr(x), _ptr(packed_W), N, K, _ptr(y), _stream(stream))
+    if check:
+        _check(st, "qgemv_run_noalloc")
     return st
 
 

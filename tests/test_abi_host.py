@@ -63,7 +63,7 @@ def test_group_sizes_and_status_strings():
     for f in synth.FORMAT_NAMES:
         assert qgemv.group_size(f) == oracle.group_size(f)
     assert qgemv.group_size(17) == 0
-    for s in range(9):
+    for s in range(10):
         assert qgemv.status_string(s) and qgemv.status_string(s) != "unknown status"
     assert qgemv.status_string(99) == "unknown status"
 
