@@ -195,6 +195,36 @@ def largest_divisor_le(k: int, cap: int) -> int:
     return 1
 
 
+def run_profile_launches(args, gemvs):
+    """Plain launches of the workload's GEMVs (one weight copy, no graph, no timing), for
+    running under a profiler: `--profile-launches N [--only LABEL]`."""
+    import torch
+
+    from quantized_weight_dequant_gb300 import qgemv
+    from quantized_weight_dequant_gb300.build import build_library
+
+    build_library()
+    h = qgemv.create(0)
+    if args.pdl:
+        qgemv.set_option(h, qgemv.OPT_PDL, 1)
+    todo = [g for g in gemvs if args.only in (None, g[0])]
+    if not todo:
+        raise SystemExit(f"--only {args.only}: no such GEMV in {args.workload}")
+    for gi, (label, fmt, N, K, _) in enumerate(todo):
+        W = torch.from_numpy(synth.make_weights(fmt, N, K, synth.config_seed(1, gi))).cuda()
+        x = torch.from_numpy(synth.make_x(fmt, K, synth.config_seed(1, gi)).view(np.int16).copy()).cuda()
+        y = torch.empty(N, dtype=torch.float32, device="cuda")
+        for _ in range(args.profile_launches):
+            qgemv.run(h, fmt, x, W, N, K, y)
+        torch.cuda.synchronize()
+        st = qgemv.check_error(h)
+        if st != qgemv.OK:
+            raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
+        print(f"{label}: {args.profile_launches} launches, {qgemv.describe(h, fmt, N, K)}", flush=True)
+    h.close()
+    return 0
+
+
 def run_ours(args, gemvs, rank, world):
     import torch
 
@@ -252,11 +282,7 @@ def run_ours(args, gemvs, rank, world):
     with torch.cuda.graph(g, stream=stream):
         for i in range(spg):
             step(i, stream)
-    launches_per_step = 0
-    for _, f, n, k, _ in gemvs:
-        d = qgemv.describe(h, f, n, k)
-        split = int(d.split("splitk=")[1].split()[0]) if "splitk=" in d else 1
-        launches_per_step += 1 + (1 if split > 1 else 0)
+    launches_per_step = len(gemvs)  # one kernel per GEMV (split-K adds its column sums in-kernel)
 
     # warm-up: at least W steps
     warm_reps = max(1, math.ceil(args.warmup / spg))
@@ -363,10 +389,14 @@ def run_ours(args, gemvs, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         sampler = OracleSampler(gemvs, threads)
-        rate, dt, sample = sampler.run(args.cpu_seconds)
+        rates, spent = [], 0.0
+        while spent < args.cpu_seconds or len(rates) < 3:  # repeated bounded samples, median rate
+            rate, dt, sample = sampler.run(max(0.5, args.cpu_seconds / 5))
+            rates.append(rate)
+            spent += dt
         sampler.close()
-        cpu = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{sample}; {dt:.1f} s wall"}
+        cpu = {"value": statistics.median(rates), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{sample}; median of {len(rates)} samples, {spent:.1f} s wall in total"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -401,6 +431,9 @@ def main(argv=None):
     ap.add_argument("--pdl", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="only run this many plain launches of each GEMV (for a profiler) and exit")
+    ap.add_argument("--only", default=None, help="with --profile-launches: the one GEMV label to run")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, when known for this build")
     args = ap.parse_args(argv)
@@ -409,6 +442,8 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     gemvs = WORKLOADS[args.workload]
+    if args.profile_launches:
+        return run_profile_launches(args, gemvs)
     if args.impl == "reference":
         return run_reference(args, gemvs, rank, world)
     return run_ours(args, gemvs, rank, world)
