@@ -159,7 +159,13 @@ int qgemv_group_size(qgemv_format_t fmt);
  *                             range of rows (so it reads only that part of x) and the column
  *                             sums of a row meet in the handle's workspace, where the last
  *                             CTA of the range adds them in column order.  1: each CTA covers
- *                             every K-column of its rows and adds them in shared memory. */
+ *                             every K-column of its rows and adds them in shared memory.
+ *   QGEMV_OPT_GRID_PER_SM     0 (default): as many streaming CTAs per SM as fit, except
+ *                             that with QGEMV_OPT_PDL a launch that covers K in one CTA and
+ *                             has at most 16 rows per warp takes one CTA per SM; 1: one per
+ *                             SM; 2: two per SM.  One per SM leaves the rest of each SM to
+ *                             the next kernel of a programmatic-dependent-launch chain, whose
+ *                             CTAs then fetch their first weights while this one finishes. */
 typedef enum {
   QGEMV_OPT_FORCE_PATH = 0,
   QGEMV_OPT_RING_DEPTH = 2,
@@ -168,7 +174,8 @@ typedef enum {
   QGEMV_OPT_PDL = 5,
   QGEMV_OPT_TEST_STALL = 6,
   QGEMV_OPT_CTAS_PER_SM = 7,
-  QGEMV_OPT_KSPLIT = 8
+  QGEMV_OPT_KSPLIT = 8,
+  QGEMV_OPT_GRID_PER_SM = 9
 } qgemv_option_t;
 
 qgemv_status_t qgemv_set_option(qgemv_handle_t h, qgemv_option_t opt, int64_t value);

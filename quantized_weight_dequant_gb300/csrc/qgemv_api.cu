@@ -33,6 +33,7 @@ struct Handle {
   int* cnt = nullptr;   // split-K per-range arrival counts, zero between launches
   int ctas_per_sm = 2;
   int ksplit = 0;       // 0: split K-columns over CTAs when the workspace holds them; 1: never
+  int grid_per_sm = 0;  // CTAs launched per SM (0: as many as fit, ctas_per_sm)
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   int force_path = 0;
   int ring_depth = 0;
@@ -148,13 +149,18 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   const bool split = Wk == 1 || (h.ksplit == 0 && Wk >= 3 && static_cast<double>(N) * Wk <= static_cast<double>(kWsFloats));
   const int P = split ? kMaxWarps / cps : std::max(1, (kMaxWarps / cps) / Wk);
   const int warps = split ? P : P * Wk;
+  // Under programmatic dependent launch a fused launch with few rows per warp (at most 16
+  // with every slot filled) takes one CTA per SM: the next launch's CTAs then fit beside it
+  // and fetch their first stages while this one finishes.
+  const bool short_pdl = h.pdl && !split && cps == 2 && N <= int64_t{16} * h.sms * cps * P;
+  const int gps = h.grid_per_sm > 0 ? std::min(h.grid_per_sm, cps) : (short_pdl ? 1 : cps);
   int64_t ranges, grid;
   if (split) {
-    ranges = std::min<int64_t>(std::max(1, (h.sms * cps) / Wk), (N + P - 1) / P);
+    ranges = std::min<int64_t>(std::max(1, (h.sms * gps) / Wk), (N + P - 1) / P);
     ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));
     grid = ranges * Wk;
   } else {
-    grid = std::min<int64_t>(int64_t{h.sms} * cps, (N + P - 1) / P);
+    grid = std::min<int64_t>(int64_t{h.sms} * gps, (N + P - 1) / P);
     if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
     grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
     ranges = grid;
@@ -168,8 +174,9 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   const int slice = slice_of(f);
   // Defaults: 2 rows per stage, 4 stages; split launches (long K): 4 rows, 2 stages.
   const bool long_k = split && Wk > 1;
-  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : (long_k ? 4 : 2);
-  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : (long_k ? 2 : 4);
+  const bool half = gps < cps;  // one CTA per SM of a two-per-SM layout
+  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : (long_k || half ? 4 : 2);
+  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : (long_k ? 2 : half ? 3 : 4);
   const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
   auto limit = [&](int d, int r) { return std::min(h.dyn_smem_max[f][r_index(r)][d_index(d)], cap); };
   auto smem_of = [&](int d, int r) { return stream_smem(warps, d, r, slice, Wk, red_rows, Kx).total; };
@@ -368,6 +375,10 @@ qgemv_status_t qgemv_set_option(qgemv_handle_t hh, qgemv_option_t opt, int64_t v
     case QGEMV_OPT_CTAS_PER_SM:
       if (v < 1 || v > 2) return QGEMV_ERR_INVALID_ARG;
       h->ctas_per_sm = static_cast<int>(v);
+      return QGEMV_OK;
+    case QGEMV_OPT_GRID_PER_SM:
+      if (v < 0 || v > 2) return QGEMV_ERR_INVALID_ARG;
+      h->grid_per_sm = static_cast<int>(v);
       return QGEMV_OK;
     case QGEMV_OPT_KSPLIT:
       if (v < 0 || v > 1) return QGEMV_ERR_INVALID_ARG;

@@ -38,8 +38,6 @@ __device__ __forceinline__ float h2f(uint32_t bits16) {
 }
 __device__ __forceinline__ float bf2f(uint32_t bits16) { return __uint_as_float((bits16 & 0xFFFFu) << 16); }
 __device__ __forceinline__ float p2(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
-__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
-__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
 
 constexpr float kTwo24 = 16777216.0f;
 
@@ -99,11 +97,14 @@ __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// 32 staged values (one chunk).  Loaded with volatile shared loads: the registers they fill
+// must stay live for the whole kernel, and a plain load could be re-executed on every stage
+// instead (rematerialised from the staging buffer).
 __device__ __forceinline__ void ld_chunk(const uint16_t* q, uint32_t (&v)[16]) {
-  const uint4* p = reinterpret_cast<const uint4*>(q);
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(q));
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4 a = p[i];
+    const uint4 a = lds_v4(sa + 16 * i);
     v[4 * i] = a.x, v[4 * i + 1] = a.y, v[4 * i + 2] = a.z, v[4 * i + 3] = a.w;
   }
 }
@@ -167,10 +168,14 @@ struct IntX {
       ld_chunk(X.q + k1, b);
 #pragma unroll
       for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
-      xf0 = X.e[k0 >> 5];
-      xf1 = X.e[k1 >> 5];
-      xsi[0] = X.s[k0 >> 4], xsi[1] = X.s[(k0 >> 4) + 1];
-      xsi[2] = X.s[k1 >> 4], xsi[3] = X.s[(k1 >> 4) + 1];
+      const uint32_t ea = static_cast<uint32_t>(__cvta_generic_to_shared(X.e));
+      const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(X.s));
+      xf0 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5)));
+      xf1 = __uint_as_float(lds_u32(ea + 4 * (k1 >> 5)));
+      xsi[0] = static_cast<int>(lds_u32(sa + 4 * (k0 >> 4)));
+      xsi[1] = static_cast<int>(lds_u32(sa + 4 * (k0 >> 4) + 4));
+      xsi[2] = static_cast<int>(lds_u32(sa + 4 * (k1 >> 4)));
+      xsi[3] = static_cast<int>(lds_u32(sa + 4 * (k1 >> 4) + 4));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) xr[i] = 0u;
@@ -193,12 +198,14 @@ struct DecQ4K : IntX {
   static constexpr int kSB = 144, kSB2 = 0;
   int c;
   uint32_t sel_s, sel_h, m1, m2, shm;
+  uint32_t qoff;   // byte offset of this lane's quants in a block
   float xs0, xs1;  // activation sums of the two groups
 
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
 
   __device__ __forceinline__ void init(int c_) {
     c = c_;
+    qoff = 16 + 32 * c;
     const int j = 2 * (c & 1);  // byte index of group 2c within its scale word
     // c < 2: s = S[2c], S[2c+1] & 63 (word h.y); c >= 2: low nibbles of S[2c+4], S[2c+5]
     // (word h.w) with bits 6..7 of S[2c-4], S[2c-3] (word h.y) above them.
@@ -231,10 +238,18 @@ struct DecQ4K : IntX {
     return fmaf(t0, xf0, t1 * xf1);
   }
 
-  __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
-    const uint4 h = *reinterpret_cast<const uint4*>(blk);
-    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+  // blk: shared-window address of the row's superblock slice (16-byte aligned).
+  // Two phases, so that a stage's rows are all loaded before any is computed: fetch() reads
+  // the lane's 48 bytes of the row from the ring, compute() needs no shared memory.
+  struct Raw {
+    uint4 h, q0, q1;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const {
+    const uint32_t q = blk + qoff;
+    return Raw{lds_v4_at<0>(blk), lds_v4_at<0>(q), lds_v4_at<16>(q)};
+  }
+  __device__ __forceinline__ float compute(const Raw& R_) const {
+    const uint4 h = R_.h, q0 = R_.q0, q1 = R_.q1;
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
@@ -273,12 +288,17 @@ struct DecQ5K : DecQ4K {
     rh = (3u - 2u * c_) & 31u;
   }
 
-  __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
-    const uint4 h = *reinterpret_cast<const uint4*>(blk);
-    const uint4 e0 = *reinterpret_cast<const uint4*>(blk + 16);
-    const uint4 e1 = *reinterpret_cast<const uint4*>(blk + 32);
-    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
-    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 64 + 32 * c);
+  struct Raw {
+    uint32_t b;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
+  __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
+  __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
+    const uint4 h = lds_v4(blk);
+    const uint4 e0 = lds_v4(blk + 16);
+    const uint4 e1 = lds_v4(blk + 32);
+    const uint4 qa = lds_v4(blk + 48 + 32 * c);
+    const uint4 qb = lds_v4(blk + 64 + 32 * c);
     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
     int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
@@ -326,14 +346,21 @@ struct DecQ6K : IntX {
     xf1 *= 1.0f / kTwo24;
   }
 
-  __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
+  // blk: shared-window address of the row's superblock (2-byte aligned: 210-byte blocks).
+  struct Raw {
+    uint32_t b;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
+  __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
+  __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
     const int H = c >> 1, rr = c & 1;
-    const uint8_t* ql = blk + 64 * H + 32 * rr;
-    const uint8_t* qh = blk + 128 + 32 * H;
+    const uint32_t ql = blk + 64 * H + 32 * rr;
+    const uint32_t qh = blk + 128 + 32 * H;
     int acc[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t l = ld_u32_a2(ql + 4 * u), e = ld_u32_a2(qh + 4 * u);
+      const uint32_t l = lds_u16(ql + 4 * u) | (lds_u16(ql + 4 * u + 2) << 16);
+      const uint32_t e = lds_u16(qh + 4 * u) | (lds_u16(qh + 4 * u + 2) << 16);
       const uint32_t lo6 = (l & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rlo) & 0x30303030u);
       const uint32_t hi6 = ((l >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rhi) & 0x30303030u);
       const int g = u >> 2;
@@ -342,12 +369,12 @@ struct DecQ6K : IntX {
       acc[2 + g] = dp2a_lo_u(xr[16 + 2 * u], hi6, acc[2 + g]);
       acc[2 + g] = dp2a_hi_u(xr[16 + 2 * u + 1], hi6, acc[2 + g]);
     }
-    const int8_t* sc = reinterpret_cast<const int8_t*>(blk + 192 + 8 * H + 2 * rr);
-    const float d = h2f(ld_u16(blk + 208));
-    const float r0 = fmaf(static_cast<float>(sc[0]), static_cast<float>(acc[0] - xsi[0]),
-                          static_cast<float>(sc[1]) * static_cast<float>(acc[1] - xsi[1]));
-    const float r1 = fmaf(static_cast<float>(sc[4]), static_cast<float>(acc[2] - xsi[2]),
-                          static_cast<float>(sc[5]) * static_cast<float>(acc[3] - xsi[3]));
+    const uint32_t sc = blk + 192 + 8 * H + 2 * rr;
+    const float d = h2f(lds_u16(blk + 208));
+    const float r0 = fmaf(static_cast<float>(lds_s8(sc)), static_cast<float>(acc[0] - xsi[0]),
+                          static_cast<float>(lds_s8(sc + 1)) * static_cast<float>(acc[1] - xsi[1]));
+    const float r1 = fmaf(static_cast<float>(lds_s8(sc + 4)), static_cast<float>(acc[2] - xsi[2]),
+                          static_cast<float>(lds_s8(sc + 5)) * static_cast<float>(acc[3] - xsi[3]));
     return d * fmaf(r0, xf0, r1 * xf1);
   }
 };
@@ -367,20 +394,25 @@ struct DecQ80 : IntX {
     xf1 *= 1.0f / kTwo24;
   }
 
-  __device__ __forceinline__ float row(const uint8_t* sblk, const uint8_t*) const {
+  struct Raw {
+    uint32_t b;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
+  __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
+  __device__ __forceinline__ float row(uint32_t sblk, uint32_t) const {
     float r[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const uint8_t* blk = sblk + 34 * (2 * c + e);
+      const uint32_t blk = sblk + 34 * (2 * c + e);
       int a0 = 0, a1 = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const uint32_t wd = ld_u32_a2(blk + 2 + 4 * u);
+        const uint32_t wd = lds_u16(blk + 2 + 4 * u) | (lds_u16(blk + 4 + 4 * u) << 16);
         int& a = (u & 1) ? a1 : a0;
         a = dp2a_lo_s(xr[16 * e + 2 * u], wd, a);
         a = dp2a_hi_s(xr[16 * e + 2 * u + 1], wd, a);
       }
-      r[e] = h2f(ld_u16(blk)) * static_cast<float>(a0 + a1);
+      r[e] = h2f(lds_u16(blk)) * static_cast<float>(a0 + a1);
     }
     return fmaf(r[0], xf0, r[1] * xf1);
   }
@@ -423,8 +455,9 @@ struct DecNVFP4 {
       ld_chunk(X.q + k0 + 32, b);
 #pragma unroll
       for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
-      xf0 = X.e[k0 >> 5];
-      xf1 = X.e[(k0 >> 5) + 1];
+      const uint32_t ea = static_cast<uint32_t>(__cvta_generic_to_shared(X.e));
+      xf0 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5)));
+      xf1 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5) + 4));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) xr[i] = 0u;
@@ -443,11 +476,17 @@ struct DecNVFP4 {
     return h;
   }
 
-  __device__ __forceinline__ float row(const uint8_t* nib, const uint8_t* sc) const {
-    const uint4 q0 = *reinterpret_cast<const uint4*>(nib + 32 * c);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(nib + 32 * c + 16);
+  struct Raw {
+    uint4 q0, q1;
+    uint32_t s4;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t nib, uint32_t sc) const {
+    return Raw{lds_v4(nib + 32 * c), lds_v4(nib + 32 * c + 16), lds_u32(sc + 4 * c)};
+  }
+  __device__ __forceinline__ float compute(const Raw& R_) const {
+    const uint4 q0 = R_.q0, q1 = R_.q1;
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const uint32_t s4 = *reinterpret_cast<const uint32_t*>(sc + 4 * c) & 0x7F7F7F7Fu;  // |scale|
+    const uint32_t s4 = R_.s4 & 0x7F7F7F7Fu;  // |scale|
     float r[2] = {0.f, 0.f};
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -492,6 +531,7 @@ struct DecTQ10 {
   __device__ __forceinline__ void init(int c_) { c = c_; }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     xsum = 0.f;
+    const uint32_t qa = static_cast<uint32_t>(__cvta_generic_to_shared(X.q));
 #pragma unroll
     for (int i = 0; i < 13; ++i) {
       const int p = 13 * c_ + i;
@@ -499,7 +539,7 @@ struct DecTQ10 {
 #pragma unroll
       for (int n = 0; n < 5; ++n) {
         const bool has = active && !(p >= 48 && n == 4);
-        y[n] = has ? h2f(X.q[256 * sbcol + elem_of(p, n)]) : 0.f;
+        y[n] = has ? h2f(lds_u16(qa + 2 * (256 * sbcol + elem_of(p, n)))) : 0.f;
         xsum += y[n];
       }
       y[5] = 0.f;
@@ -508,12 +548,17 @@ struct DecTQ10 {
     }
   }
 
-  __device__ __forceinline__ float row(const uint8_t* blk, const uint8_t*) const {
+  struct Raw {
+    uint32_t b;
+  };
+  __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
+  __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
+  __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
     constexpr float kMagic = 8388608.0f;  // 2^23
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int i = 0; i < 13; ++i) {
-      const float b = static_cast<float>(blk[13 * c + i]);
+      const float b = static_cast<float>(lds_u8(blk + 13 * c + i));
       float& a = (i & 1) ? a1 : a0;
       a = fmaf(g[i][0], __fmaf_rd(b, 3.f / 256.f, kMagic) - kMagic, a);
       a = fmaf(g[i][1], __fmaf_rd(b, 9.f / 256.f, kMagic) - kMagic, a);
@@ -521,7 +566,7 @@ struct DecTQ10 {
       a = fmaf(g[i][3], __fmaf_rd(b, 81.f / 256.f, kMagic) - kMagic, a);
       a = fmaf(g[i][4], __fmaf_rd(b, 243.f / 256.f, kMagic) - kMagic, a);
     }
-    const float d = h2f(ld_u16(blk + 52));
+    const float d = h2f(lds_u16(blk + 52));
     return d * ((a0 + a1) - xsum);
   }
 };

@@ -180,38 +180,42 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   for (int j = 0; j < J1; ++j) ok1[j] = lane + 32 * j < n1;
 #pragma unroll
   for (int j = 0; j < J2; ++j) ok2[j] = lane + 32 * j < n2;
-  const uint8_t* src1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
-  const uint8_t* src2 = (SB2 > 0) ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane : a.W;
-  const uint32_t dst0 = smem_u32(ring) + 16 * lane;
-  const int nst = (nrows + R - 1) / R;
+  // Rows of a stage are requested in order through running pointers; row bytes fit in 32 bits.
+  const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
+  const uint8_t* gi1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
+  const uint8_t* gi2 = (SB2 > 0) ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane : a.W;
+  const uint32_t ring_sa = smem_u32(ring), ring_end = ring_sa + D * STAGE;
+  const int nst = (nrows + R - 1) / R, nfull = nrows / R, tail = nrows - nfull * R;
 
-  // Requests stage st into ring slot `slot`: rows st * R + r of the row group, clamped to
-  // the last row (a short last stage re-reads that row into its spare slots; those rows
-  // are decoded and dropped), so no copy needs a row test.
-  auto issue = [&](int st, int slot) {
-    if (st < nst) {
-      const uint32_t dst = dst0 + slot * STAGE;
+  // This lane's copies of one row slice: to shared address d, from row pointers s1 / s2.
+  auto copy_row = [&](uint32_t d, const uint8_t* s1, const uint8_t* s2) {
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int64_t row = min(st * R + r, nrows - 1);
-        const uint8_t* s1 = src1 + row * a.row_bytes;
-        const uint32_t d = dst + r * SLICE;
-#pragma unroll
-        for (int j = 0; j < J1; ++j) {
-          switch (j) {  // immediate offsets: 512 j
-            case 0: cp_async16_if<0, 0>(d, s1, ok1[j]); break;
-            case 1: cp_async16_if<512, 512>(d, s1, ok1[j]); break;
-            case 2: cp_async16_if<1024, 1024>(d, s1, ok1[j]); break;
-            case 3: cp_async16_if<1536, 1536>(d, s1, ok1[j]); break;
-            case 4: cp_async16_if<2048, 2048>(d, s1, ok1[j]); break;
-          }
-        }
-        if (SB2 > 0) {
-          const uint8_t* s2 = src2 + row * a.row_bytes2;
-#pragma unroll
-          for (int j = 0; j < J2; ++j) cp_async16_if<8 * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
-        }
+    for (int j = 0; j < J1; ++j) {
+      switch (j) {  // immediate offsets: 512 j
+        case 0: cp_async16_if<0, 0>(d, s1, ok1[j]); break;
+        case 1: cp_async16_if<512, 512>(d, s1, ok1[j]); break;
+        case 2: cp_async16_if<1024, 1024>(d, s1, ok1[j]); break;
+        case 3: cp_async16_if<1536, 1536>(d, s1, ok1[j]); break;
+        case 4: cp_async16_if<2048, 2048>(d, s1, ok1[j]); break;
       }
+    }
+    if (SB2 > 0) {
+#pragma unroll
+      for (int j = 0; j < J2; ++j) cp_async16_if<8 * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
+    }
+  };
+  // Requests stage st (issued in order) into the ring slot at shared address slot_sa: R rows,
+  // or the `tail` rows of the short last stage (its other slots keep stale bytes, which are
+  // decoded and dropped).
+  auto issue = [&](int st, uint32_t slot_sa) {
+    const uint32_t d = slot_sa + 16 * lane;
+    if (st < nfull) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) copy_row(d + r * SLICE, gi1 + r * rb1, gi2 + r * rb2);
+      gi1 += R * rb1;
+      gi2 += R * rb2;
+    } else if (st < nst) {
+      for (int r = 0; r < tail; ++r) copy_row(d + r * SLICE, gi1 + r * rb1, gi2 + r * rb2);
     }
     cp_async_commit();
   };
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   };
   if (a.pdl) {
 #pragma unroll 1
-    for (int s = 0; s < D - 1; ++s) issue(s, s);
+    for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
     pdl_wait();
     issue_x();
     cp_async_wait<0>();
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     pdl_wait();  // returns at once: this launch does not overlap the previous kernel
     issue_x();
 #pragma unroll 1
-    for (int s = 0; s < D - 1; ++s) issue(s, s);
+    for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
     cp_async_wait<D - 1>();
   }
   QG_TRACE(1);
@@ -256,31 +260,37 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   dec.init(lane & 3);
   dec.load_x(X, 8 * (wk - kc0) + col, lane & 3, active);  // superblock index within the buffer
 
-  int slot = 0;  // ring slot of stage st; stage st + D - 1 goes to the slot freed by st - 1
+  // Where row sums go: y (one K-column), the workspace (split mode) or the CTA's reduction
+  // buffer (fused mode, stride Wk).
+  float* const out = a.Wk == 1 ? a.y + p_lo
+                     : a.split ? a.ws + wk * a.N + p_lo
+                               : red + static_cast<int>(p_lo - r_lo) * a.Wk + wk;
+  const int ostride = (a.Wk == 1 || a.split) ? 1 : a.Wk;
+
+  uint32_t cs = ring_sa;                     // slot of stage st
+  uint32_t is = ring_sa + (D - 1) * STAGE;   // slot for stage st + D - 1 (freed by st - 1)
+  const uint32_t lo1 = col * SB, lo2 = 8 * SB + col * SB2;  // this lane's superblock in a row slice
+  const bool writer = lane % LPR == 0;
+  float* optr = out + (lane / LPR) * ostride;
   for (int st = 0; st < nst; ++st) {
-    issue(st + D - 1, slot == 0 ? D - 1 : slot - 1);
+    issue(st + D - 1, is);
     cp_async_wait<D - 1>();
     __syncwarp();
     if (st == 0) QG_TRACE(3);
-    const uint8_t* s1 = ring + slot * STAGE + col * SB;
-    const uint8_t* s2 = ring + slot * STAGE + 8 * SB + col * SB2;
+    typename Dec::Raw raw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) raw[r] = dec.fetch(cs + lo1 + r * SLICE, cs + lo2 + r * SLICE);
     float v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) v[r] = dec.row(s1 + r * SLICE, s2 + r * SLICE);
+    for (int r = 0; r < R; ++r) v[r] = dec.compute(raw[r]);
     __syncwarp();  // every lane is done with this slot before it is refilled
-    slot = (slot == D - 1) ? 0 : slot + 1;
+    is = cs;
+    cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;
 #pragma unroll
     for (int r = 0; r < R; ++r) v[r] = active ? v[r] : 0.f;
     const float sum = reduce_rows<R>(v, lane);
-    const int row = st * R + lane / LPR;
-    if (lane % LPR == 0 && row < nrows) {
-      if (a.Wk == 1)
-        a.y[p_lo + row] = sum;
-      else if (a.split)
-        a.ws[wk * a.N + p_lo + row] = sum;
-      else
-        red[(p_lo - r_lo + row) * a.Wk + wk] = sum;
-    }
+    if (writer && st * R + lane / LPR < nrows) *optr = sum;
+    optr += R * ostride;
   }
   cp_async_wait<0>();
   QG_TRACE(4);

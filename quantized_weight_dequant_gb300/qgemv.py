@@ -13,7 +13,7 @@ from .build import LIB
 
 Q4_K, NVFP4, TQ1_0, Q5_K, Q6_K, Q8_0 = 0, 1, 2, 3, 4, 5
 OPT_FORCE_PATH, OPT_RING_DEPTH, OPT_ROWS_PER_STAGE, OPT_SPIN_LIMIT_NS, OPT_PDL, OPT_TEST_STALL, OPT_CTAS_PER_SM, \
-    OPT_KSPLIT = 0, 2, 3, 4, 5, 6, 7, 8
+    OPT_KSPLIT, OPT_GRID_PER_SM = 0, 2, 3, 4, 5, 6, 7, 8, 9
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED_FORMAT", 3: "QGEMV_ERR_BAD_SHAPE",
           4: "QGEMV_ERR_MISALIGNED", 5: "QGEMV_ERR_CUDA", 6: "QGEMV_ERR_TIMEOUT", 7: "QGEMV_ERR_OOM",
           8: "QGEMV_ERR_NO_DEVICE", 9: "QGEMV_ERR_TOO_LARGE"}
