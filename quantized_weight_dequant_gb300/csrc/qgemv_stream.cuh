@@ -308,12 +308,14 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     __shared__ int last;
     __syncthreads();  // every column sum of this CTA is written
     if (threadIdx.x == 0) {
-      __threadfence();  // ... and visible device-wide (cumulative over the barrier) before the count
-      last = atomicAdd(a.cnt + b, 1) == a.Wk - 1;
+      // acq_rel: releases the CTA's column sums (cumulative over the barrier) with the count,
+      // and acquires the other CTAs' sums for the CTA that turns out to be last.
+      int old;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.cnt + b) : "memory");
+      last = old == a.Wk - 1;
     }
     __syncthreads();
     if (last) {
-      __threadfence();
       for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
         float v[16];  // all column sums of the row in flight at once (Wk <= 16)
 #pragma unroll
