@@ -470,6 +470,14 @@ struct DecNVFP4 {
     asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
     return h;
   }
+  // The four bytes of w (eight E2M1 codes) as four f16 pairs, byte i in h[i].
+  __device__ __forceinline__ static void e2m1x8(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+  }
   __device__ __forceinline__ static uint32_t e4m3x2(uint32_t two) {
     uint32_t h;
     asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(two));
@@ -494,10 +502,12 @@ struct DecNVFP4 {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint32_t wd = w[2 * b + u];
-        fma2h(a0, a1, xr[8 * b + 4 * u + 0], e2m1x2(wd & 0xFFu));
-        fma2h(a2, a3, xr[8 * b + 4 * u + 1], e2m1x2((wd >> 8) & 0xFFu));
-        fma2h(a0, a1, xr[8 * b + 4 * u + 2], e2m1x2((wd >> 16) & 0xFFu));
-        fma2h(a2, a3, xr[8 * b + 4 * u + 3], e2m1x2(wd >> 24));
+        uint32_t hw[4];
+        e2m1x8(wd, hw);
+        fma2h(a0, a1, xr[8 * b + 4 * u + 0], hw[0]);
+        fma2h(a2, a3, xr[8 * b + 4 * u + 1], hw[1]);
+        fma2h(a0, a1, xr[8 * b + 4 * u + 2], hw[2]);
+        fma2h(a2, a3, xr[8 * b + 4 * u + 3], hw[3]);
       }
       const float sv = h2f(e4m3x2((s4 >> (8 * b)) & 0xFFu));
       r[b >> 1] = fmaf(sv, (a0 + a1) + (a2 + a3), r[b >> 1]);
@@ -507,17 +517,21 @@ struct DecNVFP4 {
 };
 
 // ------------------------------------------------------------------------------- TQ1_0
-// Lane piece c = payload bytes [13c, 13c+13) of qs[48] ++ qh[4].  For a byte b whose
+// Lane piece c = qs bytes [12c, 12c+12) (three words) and qh byte c.  For a byte b whose
 // digits n = 0..4 weigh activations y_0..y_4: sum_n y_n t_n(b) = sum_{k=1..5} g_k F_k(b)
 // with F_k(b) = floor(3^k b / 256), g_k = y_{k-1} - 3 y_k, y_5 = 0; qh bytes carry four
-// digits, so their y_4 is 0 ("metal: TQ1_0 kernel performance", section 1).  F_k is one
-// round-toward-minus-infinity FMA: 2^23 + b * 3^k / 256 rounded down is 2^23 + F_k.  The
-// activations stay fp16 in the staging buffer; each lane keeps its 65 coefficients g in
-// registers as fp32.
+// digits, so their y_4 is 0 ("metal: TQ1_0 kernel performance", section 1, the zero-padded
+// collapse).  Here everything is integer: the activations are 13-bit fixed point with one
+// exponent per superblock, so every g_k fits int16; F_k of four bytes at once comes from
+// multiplying the even and the odd bytes, spread into 16-bit lanes, by 3 (k times; b 3^k <
+// 2^16 never carries into the next lane) and picking byte 1 of each lane; dp2a then takes
+// the dot products with the int16 g pairs.
 struct DecTQ10 {
   static constexpr int kSB = 54, kSB2 = 0;
-  float g[13][5];
-  float xsum;
+  uint32_t gw[3][5][2];  // [word][k-1]: g of bytes 0,1 and of bytes 2,3 as int16 pairs
+  int gq[4];             // qh byte: g_k, k = 1..4
+  int xsum;              // sum of the lane's 64 fixed-point activations
+  float xf;              // 2^-e of the superblock
   int c;
 
   __device__ __forceinline__ static int elem_of(int p, int n) {
@@ -525,27 +539,63 @@ struct DecTQ10 {
     if (p < 48) return 160 + 16 * n + (p - 32);
     return 240 + 4 * n + (p - 48);
   }
+  // 13-bit fixed point per superblock: the 32 pieces of a superblock are the 32 lanes of one
+  // warp, which share the largest magnitude by shuffles.  Same conversion as the integer
+  // formats (one mixed-precision FMA per value), with the maximum landing in [2^12, 2^13).
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
-    reinterpret_cast<uint4*>(X.q)[i] = v;
+    uint32_t m2 = vmax_u16x2(vmax_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), vmax_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e5 = static_cast<int>(m >> 10);
+    const int e = 27 - min(e5, 30);  // in [-3, 27]
+    const int e1 = min(e, 15);
+    const uint32_t s1 = static_cast<uint32_t>(e1 + 15) << 10;
+    const uint32_t s2 = s1 | (s1 << 16);
+    const float M = 1.5f * p2(23 - (e - e1));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float f0 = M, f1 = M;
+      fma2h(f0, f1, w[k], s2);
+      w[k] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
+    }
+    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((i & 31) == 0) X.e[i >> 5] = p2(-e);
   }
   __device__ __forceinline__ void init(int c_) { c = c_; }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
-    xsum = 0.f;
-    const uint32_t qa = static_cast<uint32_t>(__cvta_generic_to_shared(X.q));
+    const uint32_t qa = static_cast<uint32_t>(__cvta_generic_to_shared(X.q)) + 512u * sbcol;
+    auto xi = [&](int p, int n) -> int {
+      return active ? static_cast<int>(static_cast<int16_t>(lds_u16(qa + 2 * elem_of(p, n)))) : 0;
+    };
+    xsum = 0;
 #pragma unroll
-    for (int i = 0; i < 13; ++i) {
-      const int p = 13 * c_ + i;
-      float y[6];
+    for (int w = 0; w < 3; ++w) {
+      int g[4][5];
 #pragma unroll
-      for (int n = 0; n < 5; ++n) {
-        const bool has = active && !(p >= 48 && n == 4);
-        y[n] = has ? h2f(lds_u16(qa + 2 * (256 * sbcol + elem_of(p, n)))) : 0.f;
-        xsum += y[n];
+      for (int j = 0; j < 4; ++j) {
+        const int p = 12 * c_ + 4 * w + j;
+        int y[6];
+#pragma unroll
+        for (int n = 0; n < 5; ++n) y[n] = xi(p, n), xsum += y[n];
+        y[5] = 0;
+#pragma unroll
+        for (int k = 1; k <= 5; ++k) g[j][k - 1] = y[k - 1] - 3 * y[k];
       }
-      y[5] = 0.f;
 #pragma unroll
-      for (int k = 1; k <= 5; ++k) g[i][k - 1] = y[k - 1] - 3.f * y[k];
+      for (int k = 0; k < 5; ++k) {
+        gw[w][k][0] = (static_cast<uint32_t>(g[0][k]) & 0xFFFFu) | (static_cast<uint32_t>(g[1][k]) << 16);
+        gw[w][k][1] = (static_cast<uint32_t>(g[2][k]) & 0xFFFFu) | (static_cast<uint32_t>(g[3][k]) << 16);
+      }
     }
+    int y[5];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) y[n] = xi(48 + c_, n), xsum += y[n];
+    y[4] = 0;
+#pragma unroll
+    for (int k = 1; k <= 4; ++k) gq[k - 1] = y[k - 1] - 3 * y[k];
+    xf = active ? X.e[sbcol] : 0.f;
   }
 
   struct Raw {
@@ -553,21 +603,32 @@ struct DecTQ10 {
   };
   __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
   __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
+  // blk: shared-window address of the row's block (2-byte aligned: 54-byte blocks).
   __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
-    constexpr float kMagic = 8388608.0f;  // 2^23
-    float a0 = 0.f, a1 = 0.f;
+    const uint32_t q = blk + 12 * c;
+    int acc = 0;
 #pragma unroll
-    for (int i = 0; i < 13; ++i) {
-      const float b = static_cast<float>(lds_u8(blk + 13 * c + i));
-      float& a = (i & 1) ? a1 : a0;
-      a = fmaf(g[i][0], __fmaf_rd(b, 3.f / 256.f, kMagic) - kMagic, a);
-      a = fmaf(g[i][1], __fmaf_rd(b, 9.f / 256.f, kMagic) - kMagic, a);
-      a = fmaf(g[i][2], __fmaf_rd(b, 27.f / 256.f, kMagic) - kMagic, a);
-      a = fmaf(g[i][3], __fmaf_rd(b, 81.f / 256.f, kMagic) - kMagic, a);
-      a = fmaf(g[i][4], __fmaf_rd(b, 243.f / 256.f, kMagic) - kMagic, a);
+    for (int w = 0; w < 3; ++w) {
+      const uint32_t W = lds_u16(q + 4 * w) | (lds_u16(q + 4 * w + 2) << 16);
+      uint32_t pe = __byte_perm(W, 0u, 0x4240);  // bytes 0, 2 in 16-bit lanes
+      uint32_t po = __byte_perm(W, 0u, 0x4341);  // bytes 1, 3
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        pe *= 3u;
+        po *= 3u;
+        const uint32_t F = __byte_perm(pe, po, 0x7351);  // F_k of bytes 0..3
+        acc = dp2a_lo_u(gw[w][k][0], F, acc);
+        acc = dp2a_hi_u(gw[w][k][1], F, acc);
+      }
+    }
+    uint32_t pq = lds_u8(blk + 48 + c);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      pq *= 3u;
+      acc += gq[k] * static_cast<int>(pq >> 8);
     }
     const float d = h2f(lds_u16(blk + 52));
-    return d * ((a0 + a1) - xsum);
+    return d * static_cast<float>(acc - xsum) * xf;
   }
 };
 
