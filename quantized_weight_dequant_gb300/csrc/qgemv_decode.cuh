@@ -97,6 +97,18 @@ __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Eight words starting at a 2-byte aligned shared address: nine aligned 32-bit loads and
+// a byte permute per word (selector 0x3210 when already 4-byte aligned, 0x5432 otherwise).
+__device__ __forceinline__ void lds_words8_a2(uint32_t addr, uint32_t (&w)[8]) {
+  const uint32_t a4 = addr & ~3u;
+  const uint32_t sel = (addr & 2u) ? 0x5432u : 0x3210u;
+  uint32_t W[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) W[i] = lds_u32(a4 + 4 * i);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = __byte_perm(W[j], W[j + 1], sel);
+}
+
 // 32 staged values (one chunk).  Loaded with volatile shared loads: the registers they fill
 // must stay live for the whole kernel, and a plain load could be re-executed on every stage
 // instead (rematerialised from the staging buffer).
@@ -357,10 +369,12 @@ struct DecQ6K : IntX {
     const uint32_t ql = blk + 64 * H + 32 * rr;
     const uint32_t qh = blk + 128 + 32 * H;
     int acc[4] = {0, 0, 0, 0};
+    uint32_t lw[8], hw[8];
+    lds_words8_a2(ql, lw);
+    lds_words8_a2(qh, hw);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t l = lds_u16(ql + 4 * u) | (lds_u16(ql + 4 * u + 2) << 16);
-      const uint32_t e = lds_u16(qh + 4 * u) | (lds_u16(qh + 4 * u + 2) << 16);
+      const uint32_t l = lw[u], e = hw[u];
       const uint32_t lo6 = (l & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rlo) & 0x30303030u);
       const uint32_t hi6 = ((l >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rhi) & 0x30303030u);
       const int g = u >> 2;
@@ -405,9 +419,11 @@ struct DecQ80 : IntX {
     for (int e = 0; e < 2; ++e) {
       const uint32_t blk = sblk + 34 * (2 * c + e);
       int a0 = 0, a1 = 0;
+      uint32_t qw[8];
+      lds_words8_a2(blk + 2, qw);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const uint32_t wd = lds_u16(blk + 2 + 4 * u) | (lds_u16(blk + 4 + 4 * u) << 16);
+        const uint32_t wd = qw[u];
         int& a = (u & 1) ? a1 : a0;
         a = dp2a_lo_s(xr[16 * e + 2 * u], wd, a);
         a = dp2a_hi_s(xr[16 * e + 2 * u + 1], wd, a);
