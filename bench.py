@@ -164,7 +164,7 @@ def run_reference(args, gemvs, rank, world):
         return 0
     threads = os.cpu_count() or 1
     sampler = OracleSampler(gemvs, threads)
-    per_step = max(0.01, 120.0 / max(1, args.steps + args.warmup))
+    per_step = max(0.01, 5.0 * args.cpu_seconds / max(1, args.steps + args.warmup))  # about a minute in all
     for _ in range(args.warmup):
         sampler.run(per_step)
     rates, total, sample = [], 0.0, ""
@@ -185,6 +185,24 @@ def run_reference(args, gemvs, rank, world):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------------ multi-rank host logic
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (all ranks take part; a single rank returns its own)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, steps: int, step_bytes: int, ms: float) -> float:
+    """Weak scaling: every rank streams its own copy of the step; bytes of all ranks over the
+    slowest rank's time."""
+    return world * steps * step_bytes / (ms * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -307,15 +325,12 @@ def run_ours(args, gemvs, rank, world):
         torch.distributed.barrier()
     elapsed_ms = e0.elapsed_time(e1)
     clk = clocks.stop() if clocks else None
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     st = qgemv.check_error(h, stream)
     if st != qgemv.OK:
         raise RuntimeError(f"qgemv error after timing: {qgemv.status_string(st)}")
 
-    value = world * args.steps * step_bytes / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, args.steps, step_bytes, elapsed_ms)
     ms_per_step = elapsed_ms / args.steps
 
     # Per-GEMV duration (CUDA events around graph replays of R launches of one GEMV).
@@ -376,11 +391,8 @@ def run_ours(args, gemvs, rank, world):
         b.record(stream)
     stream.synchronize()
     e2e_ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * e2e_steps * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e = {"value": whole_job_gbs(world, e2e_steps, step_bytes, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "ms_per_step": e2e_ms / e2e_steps,
            "how": "stream-ordered: pinned x H2D, qgemv_run per GEMV, y D2H per step; weights resident"}
