@@ -239,21 +239,25 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     cp_async_commit();
   };
   if (a.pdl) {
+    // x is read with plain loads straight into the conversion: a cp.async group for it would
+    // be committed after the weight stages and could only be waited for together with them.
 #pragma unroll 1
     for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
     pdl_wait();
-    issue_x();
-    cp_async_wait<0>();
+    QG_TRACE(1);
+#pragma unroll 1
+    for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x)
+      Dec::stage_piece(__ldcg(reinterpret_cast<const uint4*>(a.x) + pc0 + i), i, X);
   } else {
     pdl_wait();  // returns at once: this launch does not overlap the previous kernel
     issue_x();
 #pragma unroll 1
     for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
     cp_async_wait<D - 1>();
-  }
-  QG_TRACE(1);
+    QG_TRACE(1);
 #pragma unroll 1
-  for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
+    for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
+  }
   __syncthreads();
   QG_TRACE(2);
   Dec dec;
