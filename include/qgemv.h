@@ -140,11 +140,12 @@ int qgemv_group_size(qgemv_format_t fmt);
  *                             streaming kernel waits for its own copies with
  *                             cp.async.wait_group, which the hardware completes.)
  *   QGEMV_OPT_PDL             1 launches the streaming kernels with programmatic dependent
- *                             launch: their weight copies may start while the previous
- *                             kernel on the stream is still running (activations are read
- *                             only after it completes), so packed_W must not be written by
- *                             the kernel launched just before.  0 (default) launches them
- *                             normally.
+ *                             launch: they may start while the previous kernel on the stream
+ *                             is still running, and a launch that leaves room on each SM
+ *                             (see QGEMV_OPT_GRID_PER_SM) requests its first weight stages
+ *                             before waiting for it; activations are read only after it
+ *                             completes.  packed_W must therefore not be written by the kernel
+ *                             launched just before.  0 (default) launches them normally.
  *   QGEMV_OPT_TEST_STALL      test hook, default 0.  1 makes warp 0 of the first CTA of every
  *                             streaming launch also wait on a barrier that nothing completes,
  *                             bounded by the spin limit, so the timeout path (error word,

@@ -204,7 +204,11 @@ qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl)
   a.err = h.err;
   a.spin_ns = h.spin_ns;
   a.test_stall = h.test_stall;
-  a.pdl = h.pdl;
+  // Under programmatic dependent launch, a launch that leaves room on each SM for the next
+  // one requests its first weight stages before waiting for the previous kernel (kernel mode
+  // 1); one that fills the SMs cannot overlap much, and takes x first (mode 2), so x is not
+  // queued behind its own weight stages.
+  a.pdl = !h.pdl ? 0 : (gps < cps ? 1 : 2);
   a.split = split ? 1 : 0;
   a.ws = h.ws;
   a.cnt = h.cnt;

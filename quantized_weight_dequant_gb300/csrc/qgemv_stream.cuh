@@ -56,7 +56,8 @@ struct StreamArgs {
   int* err;
   uint64_t spin_ns;
   int test_stall;       // 1: warp 0 of CTA 0 also waits, bounded, on a barrier nothing completes
-  int pdl;              // launched with programmatic dependent launch
+  int pdl;              // programmatic dependent launch: 0 off; 1 on, weight stages requested
+                        // before the wait for the previous kernel; 2 on, x first (as with 0)
   // Split mode (split = 1): CTA b takes K-column b % Wk of the rows of row range b / Wk, all
   // its warps on that column (P = warps).  With Wk > 1 the column sums go to ws[kc * N + row]
   // and the last CTA of a row range (counted in cnt[range], left at 0 again) adds them.
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
       cp_async16(smem_u32(X.q) + 16 * (i - pc0), reinterpret_cast<const uint4*>(a.x) + i);
     cp_async_commit();
   };
-  if (a.pdl) {
+  if (a.pdl == 1) {
     // x is read with plain loads straight into the conversion: a cp.async group for it would
     // be committed after the weight stages and could only be waited for together with them.
 #pragma unroll 1
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x)
       Dec::stage_piece(__ldcg(reinterpret_cast<const uint4*>(a.x) + pc0 + i), i, X);
   } else {
-    pdl_wait();  // returns at once: this launch does not overlap the previous kernel
+    pdl_wait();  // at once without programmatic dependent launch
     issue_x();
 #pragma unroll 1
     for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
