@@ -61,6 +61,13 @@ def lib():
         L.oracle_gemv_range.restype = ctypes.c_int
         L.oracle_gemv_range.argtypes = [ctypes.c_int, u16p, u8p, i64, i64, i64, i64, ctypes.c_void_p,
                                         ctypes.c_void_p]
+        L.oracle_silu.restype = d
+        L.oracle_silu.argtypes = [d]
+        L.oracle_gemv_general.restype = ctypes.c_int
+        L.oracle_gemv_general.argtypes = [ctypes.c_int, u16p, u8p, i64, i64, d, d, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_swiglu.restype = ctypes.c_int
+        L.oracle_swiglu.argtypes = [ctypes.c_int, u16p, u8p, u8p, i64, i64] + [ctypes.c_void_p] * 5
         _lib = L
     return _lib
 
@@ -148,3 +155,35 @@ def gemv(fmt: int, x_bits: np.ndarray, W: np.ndarray, N: int, K: int, r0: int = 
     if rc:
         raise ValueError(f"oracle_gemv_range failed ({rc})")
     return y, S
+
+
+def silu(g: float) -> float:
+    return lib().oracle_silu(float(g))
+
+
+def gemv_general(fmt: int, x_bits: np.ndarray, W: np.ndarray, N: int, K: int, alpha: float, beta: float,
+                 c=None):
+    """(y, S) in fp64: y = alpha * x.W^T + beta * c (c unused when beta == 0), S = |alpha| sum|x w|."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    cc = np.ascontiguousarray(np.zeros(N) if c is None else c, dtype=np.float64)
+    y = np.empty(N, dtype=np.float64)
+    S = np.empty(N, dtype=np.float64)
+    rc = lib().oracle_gemv_general(fmt, _ptr(x_bits), _ptr(W), N, K, float(alpha), float(beta), _ptr(cc),
+                                   _ptr(y), _ptr(S))
+    if rc:
+        raise ValueError(f"oracle_gemv_general failed ({rc})")
+    return y, S
+
+
+def swiglu(fmt: int, x_bits: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, N: int, K: int):
+    """dict of fp64 arrays h = silu(g) * u, g, u, Sg, Su for gate / up matrices Wg, Wu."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    Wg = np.ascontiguousarray(Wg, dtype=np.uint8)
+    Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
+    out = {k: np.empty(N, dtype=np.float64) for k in ("h", "g", "u", "Sg", "Su")}
+    rc = lib().oracle_swiglu(fmt, _ptr(x_bits), _ptr(Wg), _ptr(Wu), N, K, *(_ptr(out[k]) for k in
+                                                                           ("h", "g", "u", "Sg", "Su")))
+    if rc:
+        raise ValueError(f"oracle_swiglu failed ({rc})")
+    return out

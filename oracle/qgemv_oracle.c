@@ -282,3 +282,47 @@ int oracle_gemv_range(int fmt, const uint16_t* x, const uint8_t* W, int64_t N, i
   free(rows);
   return rc;
 }
+
+/* ------------------------------------------------------------------ layer epilogues
+ * The general GEMV of the Q4_K page ("What is a GEMV"): y = alpha x.W^T + beta C, which
+ * the page then fixes to alpha = 1, beta = 0.  Row n: y[n] = alpha * dot_n + beta * c[n]
+ * (c is not read when beta == 0), S[n] = |alpha| * sum_k |x_k w(n, k)|. */
+int oracle_gemv_general(int fmt, const uint16_t* x, const uint8_t* W, int64_t N, int64_t K, double alpha,
+                        double beta, const double* c, double* y, double* S) {
+  int rc = oracle_gemv_range(fmt, x, W, N, K, 0, N, y, S);
+  if (rc) return rc;
+  for (int64_t n = 0; n < N; ++n) {
+    double v = alpha * y[n];
+    if (beta != 0.0) v += beta * c[n];
+    y[n] = v;
+    if (S) S[n] = fabs(alpha) * S[n];
+  }
+  return 0;
+}
+
+/* SiLU (x * logistic(x)), the gate non-linearity of a SwiGLU MLP. */
+double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* The gated MLP input of a decoder layer (the Q4_K page's "MLPs" of each decoder layer,
+ * read as the SwiGLU of Llama/Qwen-style models): two matrices of the same format and
+ * shape share x; h[n] = silu(g_n) * u_n with g = x.Wg^T, u = x.Wu^T.  Also returns g, u and
+ * their magnitude sums (any of g, u, Sg, Su may be NULL). */
+int oracle_swiglu(int fmt, const uint16_t* x, const uint8_t* Wg, const uint8_t* Wu, int64_t N, int64_t K,
+                  double* h, double* g, double* u, double* Sg, double* Su) {
+  double* gv = (double*)malloc((size_t)N * 4 * sizeof(double));
+  if (!gv) return -2;
+  double *uv = gv + N, *sg = gv + 2 * N, *su = gv + 3 * N;
+  int rc = oracle_gemv_range(fmt, x, Wg, N, K, 0, N, gv, sg);
+  if (!rc) rc = oracle_gemv_range(fmt, x, Wu, N, K, 0, N, uv, su);
+  if (!rc) {
+    for (int64_t n = 0; n < N; ++n) {
+      h[n] = oracle_silu(gv[n]) * uv[n];
+      if (g) g[n] = gv[n];
+      if (u) u[n] = uv[n];
+      if (Sg) Sg[n] = sg[n];
+      if (Su) Su[n] = su[n];
+    }
+  }
+  free(gv);
+  return rc;
+}

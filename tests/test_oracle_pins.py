@@ -341,3 +341,63 @@ def test_generator_distributions_and_determinism():
     # about a quarter of |N(0,1)|*0.05 falls below 2^-6, the E4M3 subnormal range
     frac_sub = np.mean(2 * sf < 2.0 ** -6)
     assert 0.1 < frac_sub < 0.45
+
+
+# ---------------------------------------------------------------- layer epilogues
+def _x_values(fmt, x):
+    """Activations as fp64 by numpy / torch (not by the oracle's own decoder)."""
+    if fmt == synth.NVFP4:
+        return torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    return x.view(np.float16).astype(np.float64)
+
+
+def test_silu_is_x_times_scipy_logistic_and_has_the_odd_part_x():
+    expit = pytest.importorskip("scipy.special").expit
+    g = np.concatenate([np.linspace(-40, 40, 801), [-800.0, -1e-300, 0.0, 1e-300, 800.0]])
+    mine = np.array([oracle.silu(v) for v in g])
+    np.testing.assert_allclose(mine, g * expit(g), rtol=1e-14, atol=0)
+    assert oracle.silu(-800.0) == 0.0 and oracle.silu(800.0) == 800.0
+    # logistic(x) + logistic(-x) = 1, so silu(x) - silu(-x) = x
+    for v in np.linspace(-30, 30, 61):
+        assert abs((oracle.silu(v) - oracle.silu(-v)) - v) <= 1e-14 * max(1.0, abs(v))
+    # the slope bound the SwiGLU tolerance relies on: max |silu'| is about 1.0998 (near x = 2.4)
+    t = np.linspace(-20, 20, 40001)
+    s = np.array([oracle.silu(v) for v in t])
+    slope = np.abs(np.diff(s) / np.diff(t)).max()
+    assert 1.09 < slope < 1.1
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.Q6_K, synth.NVFP4])
+def test_general_gemv_is_alpha_times_the_dense_product_plus_beta_c(fmt):
+    N, K = 6, 512
+    W = synth.make_weights(fmt, N, K, seed=40 + fmt)
+    x = synth.make_x(fmt, K, seed=40 + fmt)
+    dense = oracle.dequant_rows(fmt, W, N, K, range(N))
+    xv = _x_values(fmt, x)
+    c = np.random.default_rng(7).normal(size=N)
+    y, S = oracle.gemv_general(fmt, x, W, N, K, -0.75, 2.5, c)
+    ref = -0.75 * (dense @ xv) + 2.5 * c
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S, 0.75 * np.abs(dense * xv).sum(1), rtol=1e-12)
+    y1, S1 = oracle.gemv_general(fmt, x, W, N, K, 1.0, 0.0, np.full(N, np.nan))  # beta = 0 never reads c
+    y0, S0 = oracle.gemv(fmt, x, W, N, K)
+    assert np.array_equal(y1, y0) and np.array_equal(S1, S0)
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.TQ1_0, synth.NVFP4])
+def test_swiglu_gates_the_up_rows_with_silu_of_the_gate_rows(fmt):
+    expit = pytest.importorskip("scipy.special").expit
+    N, K = 7, 512
+    Wg = synth.make_weights(fmt, N, K, seed=50 + fmt)
+    Wu = synth.make_weights(fmt, N, K, seed=60 + fmt)
+    x = synth.make_x(fmt, K, seed=50 + fmt)
+    xv = _x_values(fmt, x)
+    g = oracle.dequant_rows(fmt, Wg, N, K, range(N)) @ xv
+    u = oracle.dequant_rows(fmt, Wu, N, K, range(N)) @ xv
+    out = oracle.swiglu(fmt, x, Wg, Wu, N, K)
+    np.testing.assert_allclose(out["g"], g, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["u"], u, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["h"], g * expit(g) * u, rtol=1e-11, atol=1e-12)
+    # the two matrices play different roles: swapping them changes the result
+    swapped = oracle.swiglu(fmt, x, Wu, Wg, N, K)["h"]
+    assert not np.allclose(swapped, out["h"], rtol=1e-3)
