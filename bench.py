@@ -50,6 +50,46 @@ for _p, _n, _k in synth.LAYER_SHAPES:
         WORKLOADS[f"layer_{_p}_{synth.FORMAT_NAMES[_f]}"] = [(_p, _f, _n, _k, "h")]
 DEFAULT_WORKLOAD = "q4k_llama8b_decode"
 
+# Layer launches: GEMVs of a workload that carry the same group tag run as ONE
+# qgemv_run_group launch (they share x); a group listed in SWIGLU holds a gate and an up
+# matrix (in that order) combined into one output silu(gate) * up.  Untagged GEMVs run alone.
+WORKLOADS["layer_mixed_grouped"] = WORKLOADS["layer_mixed"]
+WORKLOADS["q4k_llama8b_decode_swiglu"] = [("qkv", synth.Q4_K, 6144, 4096, "h"),
+                                          ("gate", synth.Q4_K, 14336, 4096, "h"),
+                                          ("up", synth.Q4_K, 14336, 4096, "h"),
+                                          ("down", synth.Q4_K, 4096, 14336, "m")]
+GROUPS = {"layer_mixed_grouped": {"q": "qkv", "k": "qkv", "v": "qkv", "gate": "mlp", "up": "mlp"},
+          "q4k_llama8b_decode_swiglu": {"gate": "mlp", "up": "mlp"}}
+SWIGLU = {"mlp"}
+
+
+def launch_units(workload: str, gemvs):
+    """[(label, [gemv indices], swiglu)] in workload order: one entry per kernel launch."""
+    tags = GROUPS.get(workload, {})
+    units, seen = [], {}
+    for gi, g in enumerate(gemvs):
+        tag = tags.get(g[0])
+        if tag is None:
+            units.append((g[0], [gi], False))
+        elif tag in seen:
+            units[seen[tag]][1].append(gi)
+        else:
+            seen[tag] = len(units)
+            units.append((tag, [gi], tag in SWIGLU))
+    for label, idx, sw in units:
+        if sw and len(idx) != 2:
+            raise ValueError(f"{workload}: SwiGLU group {label} needs a gate and an up matrix")
+        if len({(gemvs[i][3], gemvs[i][4]) for i in idx}) != 1:
+            raise ValueError(f"{workload}: group {label} must share K and x")
+    return units
+
+
+def unit_bytes(gemvs, idx, swiglu: bool) -> int:
+    """Algorithmic bytes of one launch: packed weights, x once, the outputs (fp32)."""
+    K = gemvs[idx[0]][3]
+    outs = gemvs[idx[0]][2] if swiglu else sum(gemvs[i][2] for i in idx)
+    return sum(synth.packed_bytes(gemvs[i][1], gemvs[i][2], gemvs[i][3]) for i in idx) + 2 * K + 4 * outs
+
 
 def gemv_bytes(fmt, N, K) -> int:
     """Algorithmic bytes of one GEMV: packed weights + x (2 B/elem) + y (4 B/elem)."""
@@ -214,8 +254,8 @@ def largest_divisor_le(k: int, cap: int) -> int:
 
 
 def run_profile_launches(args, gemvs):
-    """Plain launches of the workload's GEMVs (one weight copy, no graph, no timing), for
-    running under a profiler: `--profile-launches N [--only LABEL]`."""
+    """Plain launches of the workload's launch units (one weight copy, no graph, no timing),
+    for running under a profiler: `--profile-launches N [--only LABEL]`."""
     import torch
 
     from quantized_weight_dequant_gb300 import qgemv
@@ -225,20 +265,32 @@ def run_profile_launches(args, gemvs):
     h = qgemv.create(0)
     if args.pdl:
         qgemv.set_option(h, qgemv.OPT_PDL, 1)
-    todo = [g for g in gemvs if args.only in (None, g[0])]
-    if not todo:
-        raise SystemExit(f"--only {args.only}: no such GEMV in {args.workload}")
-    for gi, (label, fmt, N, K, _) in enumerate(todo):
-        W = torch.from_numpy(synth.make_weights(fmt, N, K, synth.config_seed(1, gi))).cuda()
-        x = torch.from_numpy(synth.make_x(fmt, K, synth.config_seed(1, gi)).view(np.int16).copy()).cuda()
-        y = torch.empty(N, dtype=torch.float32, device="cuda")
+    units = [u for u in launch_units(args.workload, gemvs) if args.only in (None, u[0])]
+    if not units:
+        raise SystemExit(f"--only {args.only}: no such launch in {args.workload}")
+    grouped = set(GROUPS.get(args.workload, {}).values())
+    for label, idx, sw in units:
+        Ws, ys = [], []
+        for gi in idx:
+            _, fmt, N, K, _ = gemvs[gi]
+            Ws.append(torch.from_numpy(synth.make_weights(fmt, N, K, synth.config_seed(1, gi))).cuda())
+            ys.append(torch.empty(N, dtype=torch.float32, device="cuda"))
+        _, fmt, N, K, _ = gemvs[idx[0]]
+        x = torch.from_numpy(synth.make_x(fmt, K, synth.config_seed(1, idx[0])).view(np.int16).copy()).cuda()
         for _ in range(args.profile_launches):
-            qgemv.run(h, fmt, x, W, N, K, y)
+            if label not in grouped:
+                qgemv.run(h, fmt, x, Ws[0], N, K, ys[0])
+            elif sw:
+                qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[0], N, ys[0], packed_W_up=Ws[1], swiglu=True)])
+            else:
+                qgemv.run_group(h, x, K, [qgemv.problem(gemvs[gi][1], W, gemvs[gi][2], y)
+                                          for gi, W, y in zip(idx, Ws, ys)])
         torch.cuda.synchronize()
         st = qgemv.check_error(h)
         if st != qgemv.OK:
             raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
-        print(f"{label}: {args.profile_launches} launches, {qgemv.describe(h, fmt, N, K)}", flush=True)
+        plan = qgemv.describe(h, fmt, N, K) if label not in grouped else "grouped launch"
+        print(f"{label}: {args.profile_launches} launches, {plan}", flush=True)
     h.close()
     return 0
 
@@ -277,13 +329,31 @@ def run_ours(args, gemvs, rank, world):
             xs[(xk, K, fmt)] = torch.from_numpy(xb.view(np.int16).copy()).to(dev)
         ys.append(torch.empty(N, dtype=torch.float32, device=dev))
         del W
-    step_bytes = sum(gemv_bytes(f, n, k) for _, f, n, k, _ in gemvs)
+    units = launch_units(args.workload, gemvs)
+    grouped = set(GROUPS.get(args.workload, {}).values())
+    for label, idx, sw in units:
+        if sw:
+            ys[idx[1]] = None  # the up matrix of a SwiGLU pair has no output of its own
+    step_bytes = sum(unit_bytes(gemvs, idx, sw) for _, idx, sw in units)
     stream = torch.cuda.Stream(device=dev)
+
+    def launch(ui, c, s):
+        """Launch unit ui on weight copy c."""
+        label, idx, sw = units[ui]
+        _, fmt, N, K, xk = gemvs[idx[0]]
+        x = xs[(xk, K, fmt)]
+        if label not in grouped:
+            qgemv.run(h, fmt, x, Ws[idx[0]][c], N, K, ys[idx[0]], stream=s)
+        elif sw:
+            qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[idx[0]][c], N, ys[idx[0]], packed_W_up=Ws[idx[1]][c],
+                                                    swiglu=True)], stream=s)
+        else:
+            qgemv.run_group(h, x, K, [qgemv.problem(gemvs[i][1], Ws[i][c], gemvs[i][2], ys[i]) for i in idx], stream=s)
 
     def step(i, s):
         c = i % copies
-        for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
-            qgemv.run(h, fmt, xs[(xk, K, fmt)], Ws[gi][c], N, K, ys[gi], stream=s)
+        for ui in range(len(units)):
+            launch(ui, c, s)
 
     # sanity: one step, checked for errors, before anything is captured
     with torch.cuda.stream(stream):
@@ -300,7 +370,7 @@ def run_ours(args, gemvs, rank, world):
     with torch.cuda.graph(g, stream=stream):
         for i in range(spg):
             step(i, stream)
-    launches_per_step = len(gemvs)  # one kernel per GEMV (split-K adds its column sums in-kernel)
+    launches_per_step = len(units)  # one kernel per launch unit (split-K adds its column sums in-kernel)
 
     # warm-up: at least W steps
     warm_reps = max(1, math.ceil(args.warmup / spg))
@@ -333,14 +403,14 @@ def run_ours(args, gemvs, rank, world):
     value = whole_job_gbs(world, args.steps, step_bytes, elapsed_ms)
     ms_per_step = elapsed_ms / args.steps
 
-    # Per-GEMV duration (CUDA events around graph replays of R launches of one GEMV).
+    # Per-launch duration (CUDA events around graph replays of R launches of one unit).
     per_call = {}
-    for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
+    for ui, (label, idx, sw) in enumerate(units):
         R = 200
         gg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gg, stream=stream):
             for i in range(R):
-                qgemv.run(h, fmt, xs[(xk, K, fmt)], Ws[gi][i % copies], N, K, ys[gi], stream=stream)
+                launch(ui, i % copies, stream)
         with torch.cuda.stream(stream):
             gg.replay()
         stream.synchronize()
@@ -354,14 +424,18 @@ def run_ours(args, gemvs, rank, world):
             stream.synchronize()
             samples.append(a.elapsed_time(b) * 1e3 / R)
         us = statistics.median(samples)
-        per_call[label] = {"us": us, "GB/s": gemv_bytes(fmt, N, K) / (us * 1e-6) / 1e9,
-                           "shape": f"{synth.FORMAT_NAMES[fmt]} {N}x{K}", "plan": qgemv.describe(h, fmt, N, K)}
+        shape = " + ".join(f"{synth.FORMAT_NAMES[gemvs[i][1]]} {gemvs[i][2]}x{gemvs[i][3]}" for i in idx)
+        per_call[label] = {"us": us, "GB/s": unit_bytes(gemvs, idx, sw) / (us * 1e-6) / 1e9,
+                           "shape": shape + (" (SwiGLU pair)" if sw else "")}
+        if label not in grouped:
+            per_call[label]["plan"] = qgemv.describe(h, gemvs[idx[0]][1], gemvs[idx[0]][2], gemvs[idx[0]][3])
         del gg
-    dom = max(gemvs, key=lambda g_: gemv_bytes(g_[1], g_[2], g_[3]))[0]
+    dom = max(units, key=lambda u_: unit_bytes(gemvs, u_[1], u_[2]))[0]
     peak, peak_kind = load_peaks()
     achieved = per_call[dom]["GB/s"]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": args.traffic, "kernel": f"stream_kernel {per_call[dom]['shape']}",
+                "traffic": args.traffic,
+                "kernel": f"{'group_kernel' if dom in grouped else 'stream_kernel'} {per_call[dom]['shape']}",
                 "peak_kind": f"hbm_gbs of {peak_kind} (copy bandwidth)",
                 "achieved_how": "algorithmic bytes per launch / mean launch duration over graph replays of 200 "
                                 "launches rotating weight copies (CUDA events on the launch stream)"}
@@ -369,15 +443,16 @@ def run_ours(args, gemvs, rank, world):
     # End to end through the public API: pinned host x -> device, 3 GEMVs, y -> pinned host.
     e2e_steps = min(args.steps, 2000)
     hx = {k: torch.from_numpy(v.view(np.int16).copy()).pin_memory() for k, v in xbits.items()}
-    hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in ys]
+    outs = [y for y in ys if y is not None]
+    hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in outs]
     h2d = sum(2 * k[1] for k in hx)
-    d2h = sum(4 * y.numel() for y in ys)
+    d2h = sum(4 * y.numel() for y in outs)
     with torch.cuda.stream(stream):
         for i in range(5):
             for k in hx:
                 xs[k].copy_(hx[k], non_blocking=True)
             step(i, stream)
-            for y, hyy in zip(ys, hy):
+            for y, hyy in zip(outs, hy):
                 hyy.copy_(y, non_blocking=True)
         stream.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,7 +461,7 @@ def run_ours(args, gemvs, rank, world):
             for k in hx:
                 xs[k].copy_(hx[k], non_blocking=True)
             step(i, stream)
-            for y, hyy in zip(ys, hy):
+            for y, hyy in zip(outs, hy):
                 hyy.copy_(y, non_blocking=True)
         b.record(stream)
     stream.synchronize()
@@ -395,7 +470,8 @@ def run_ours(args, gemvs, rank, world):
     e2e = {"value": whole_job_gbs(world, e2e_steps, step_bytes, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "ms_per_step": e2e_ms / e2e_steps,
-           "how": "stream-ordered: pinned x H2D, qgemv_run per GEMV, y D2H per step; weights resident"}
+           "how": "stream-ordered: pinned x H2D, one qgemv_run / qgemv_run_group per launch unit, "
+                  "outputs D2H per step; weights resident"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -420,6 +496,8 @@ def run_ours(args, gemvs, rank, world):
                            "l2": f"inputs larger than L2: {copies} rotating weight copies = "
                                  f"{copies * step_w_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
                            "timing": f"CUDA graph of {spg} steps replayed {reps}x, CUDA events",
+                           "launches": [f"{u_[0]}:{'+'.join(gemvs[i][0] for i in u_[1])}"
+                                        + (":swiglu" if u_[2] else "") for u_ in units],
                            "pdl": bool(args.pdl)},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,

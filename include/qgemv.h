@@ -190,6 +190,61 @@ qgemv_status_t qgemv_describe(qgemv_handle_t h, qgemv_format_t fmt, int64_t N, i
 /* Compile-time build marker, checked by the Python binding at load (provenance). */
 const char* qgemv_build_marker(void);
 
+/* ---------------------------------------------------------------- layer entry points
+ * The general form of the GEMV, y = alpha x.W^T + beta C (Q4_K page, section "What is a
+ * GEMV", with C the output's previous contents), and launches over several matrices that
+ * share one activation vector: the projections of a decoder layer that read the same x
+ * (Q, K and V; the MLP's gate and up), which that page names as the GEMVs of each decoder
+ * layer.  The MLP's gate/up pair can be combined as SwiGLU, h = silu(x.Wg^T) * (x.Wu^T)
+ * with silu(g) = g / (1 + e^-g) (the gate of Llama/Qwen-style MLPs; the pages name the MLP
+ * projections but not their activation). */
+
+/* Output element types: fp32, or fp16 / bf16 rounded to nearest even from the fp32 result. */
+typedef enum { QGEMV_OUT_F32 = 0, QGEMV_OUT_F16 = 1, QGEMV_OUT_BF16 = 2 } qgemv_out_t;
+
+/* One matrix of qgemv_run_group.  For row n < N, with r the fp32 result of the row:
+ *   swiglu = 0:  r = x . dequant(packed_W)[n, :]
+ *   swiglu = 1:  r = silu(x . dequant(packed_W)[n, :]) * (x . dequant(packed_W_up)[n, :])
+ *   y[n] = alpha * r + beta * y[n]    (y is not read when beta == 0; one rounding to `out`)
+ * packed_W (and packed_W_up): device, qgemv_packed_bytes(fmt, N, K) bytes each, 16-byte
+ * aligned; packed_W_up is ignored unless swiglu = 1.  y: device, N elements of type `out`,
+ * 16-byte aligned, not overlapping x, any matrix or another problem's y. */
+typedef struct {
+  qgemv_format_t fmt;
+  const void* packed_W;
+  const void* packed_W_up;
+  int64_t N;
+  void* y;
+  float alpha;
+  float beta;
+  qgemv_out_t out;
+  int swiglu;
+} qgemv_problem_t;
+
+/* Maximum number of matrices in one qgemv_run_group call. */
+#define QGEMV_MAX_GROUP 8
+
+/* Runs `count` (1..QGEMV_MAX_GROUP) GEMVs that share x and K, as described by problems[]
+ * (host array, read during the call only).  Formats may differ, except that x is bf16 when
+ * the matrices are NVFP4 and fp16 otherwise, so NVFP4 cannot be mixed with the other
+ * formats (QGEMV_ERR_INVALID_ARG).  K must be a multiple of every format's block length.
+ * Matrices the streaming kernel takes (K a multiple of 256 and 16-byte rows) run in ONE
+ * launch, each on a share of the CTAs in proportion to its bytes; the others get a
+ * warp-per-row launch each.  Validation as qgemv_run for every matrix, all before any
+ * launch; also INVALID_ARG for count out of range, a NULL problems, x or y, swiglu not 0/1,
+ * swiglu = 1 without packed_W_up, or `out` out of range.  Asynchronous on `stream`, no
+ * allocation; uses the handle's workspace like qgemv_run (one call at a time per handle).
+ * Deterministic like qgemv_run. */
+qgemv_status_t qgemv_run_group(qgemv_handle_t h, const void* x, int64_t K, int count,
+                               const qgemv_problem_t* problems, cudaStream_t stream);
+
+/* y = alpha * x . dequant(W)^T + beta * y for one matrix, y of type `out`: qgemv_run_group
+ * with one problem (swiglu = 0).  alpha = 1, beta = 0, out = QGEMV_OUT_F32 computes what
+ * qgemv_run does (through the grouped kernel, so the last bits may differ). */
+qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x, const void* packed_W,
+                            int64_t N, int64_t K, float alpha, float beta, void* y, qgemv_out_t out,
+                            cudaStream_t stream);
+
 /* Capacity of qgemv_run_noalloc's scratch, in fp32 column sums: N * ceil(K / 2048) of them. */
 #define QGEMV_NOALLOC_MAX_COLUMN_SUMS 262144
 

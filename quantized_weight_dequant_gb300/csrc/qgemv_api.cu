@@ -35,6 +35,8 @@ struct Handle {
   int ksplit = 0;       // 0: split K-columns over CTAs when the workspace holds them; 1: never
   int grid_per_sm = 0;  // CTAs launched per SM (0: as many as fit, ctas_per_sm)
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
+  size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
+  size_t group1_smem_max[6][2][3] = {};  // one-format grouped kernels [format][R 2/4][D 2/3/4]
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -83,6 +85,18 @@ int group_size(int f) {
   return 0;
 }
 
+// One matrix of a launch as the planner sees it.
+struct Problem {
+  int f = 0;
+  const void* W = nullptr;
+  const void* WB = nullptr;  // SwiGLU up matrix
+  int64_t N = 0;             // outputs
+  void* y = nullptr;
+  float alpha = 1.f, beta = 0.f;
+  int ydt = 0, pair = 0;
+  bool plain() const { return alpha == 1.f && beta == 0.f && ydt == 0 && !pair; }
+};
+
 struct Plan {
   int path = 2;  // 1 streaming kernel, 2 warp-per-row kernel
   StreamArgs sa{};
@@ -90,6 +104,16 @@ struct Plan {
   size_t smem = 0;
   int rw_grid = 0, rw_block = 256;
 };
+
+// A streaming launch over several matrices sharing x: the CTAs of matrix i are
+// [cta_end[i-1], cta_end[i]).
+struct GroupPlan {
+  GroupArgs ga{};
+  int fmt = -1;  // the one format of the launch, or -1 for mixed formats
+  int grid = 0, threads = 0, R = 2, D = 4;
+  size_t smem = 0;
+};
+static_assert(kMaxGroup == QGEMV_MAX_GROUP, "grouped launch capacity");
 
 }  // namespace
 
@@ -100,6 +124,14 @@ const void* stream_kernel_q6k(int R, int D);
 const void* stream_kernel_q80(int R, int D);
 const void* stream_kernel_tq10(int R, int D);
 const void* stream_kernel_nvfp4(int R, int D);
+const void* group_kernel_r2(int D);
+const void* group_kernel_r4(int D);
+const void* group_kernel_q4k(int R, int D);
+const void* group_kernel_q5k(int R, int D);
+const void* group_kernel_q6k(int R, int D);
+const void* group_kernel_q80(int R, int D);
+const void* group_kernel_tq10(int R, int D);
+const void* group_kernel_nvfp4(int R, int D);
 }  // namespace qg
 
 namespace {
@@ -116,6 +148,20 @@ const void* stream_kernel_for(int f, int R, int D) {
   return nullptr;
 }
 
+// Grouped kernel for ring shape (R, D): the one-format kernel of format f, or (f < 0) the
+// mixed-format one.
+const void* group_kernel_for(int f, int R, int D) {
+  switch (f) {
+    case F_Q4K: return group_kernel_q4k(R, D);
+    case F_Q5K: return group_kernel_q5k(R, D);
+    case F_Q6K: return group_kernel_q6k(R, D);
+    case F_Q80: return group_kernel_q80(R, D);
+    case F_TQ10: return group_kernel_tq10(R, D);
+    case F_NVFP4: return group_kernel_nvfp4(R, D);
+  }
+  return R >= 4 ? group_kernel_r4(D) : group_kernel_r2(D);
+}
+
 int r_index(int R) { return R == 1 ? 0 : R == 2 ? 1 : 2; }
 int d_index(int D) { return D - 2; }
 
@@ -127,97 +173,189 @@ void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
 
 int slice_of(int f) { return 8 * sb_bytes(f) + 8 * sb_bytes2(f); }
 
-qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl) {
+// Packed row bytes of stream 1 / 2, or false when the streaming kernel cannot take the
+// shape (rows must be whole superblocks and 16-byte multiples, at most 16 K-columns).
+bool stream_rows(int f, int64_t K, int64_t& rb1, int64_t& rb2) {
+  if (K % 256) return false;
   const int64_t nsb = K / 256;
-  int64_t rb1 = 0, rb2 = 0;
-  if (K % 256 == 0) {
-    rb1 = (f == F_NVFP4) ? K / 2 : nsb * sb_bytes(f);
-    rb2 = (f == F_NVFP4) ? K / 16 : 0;
-  }
-  const int64_t Wk64 = (nsb + 7) / 8;
-  const bool fast_ok = (K % 256 == 0) && rb1 % 16 == 0 && rb2 % 16 == 0 && Wk64 >= 1 && Wk64 <= kMaxWarps;
-  if (!fast_ok || h.force_path == 2) {
-    rowwarp_plan(h, N, pl);
-    return QGEMV_OK;
-  }
-  const int Wk = static_cast<int>(Wk64);
+  rb1 = (f == F_NVFP4) ? K / 2 : nsb * sb_bytes(f);
+  rb2 = (f == F_NVFP4) ? K / 16 : 0;
+  const int64_t Wk = (nsb + 7) / 8;
+  return rb1 % 16 == 0 && rb2 % 16 == 0 && Wk >= 1 && Wk <= kMaxWarps;
+}
+
+// The streaming launch over the matrices `ps[0..n)` (all of them streaming-eligible, one K).
+// Every matrix gets CTAs in proportion to its bytes; the launch-wide choices (K-columns per
+// CTA, split or fused, ring shape) follow from K and the largest shared-memory need.
+// `general` selects the grouped kernel (epilogue, pairs, several formats), whose ring shapes
+// are R in {2, 4}.  Returns false when no ring shape fits (the caller falls back).
+bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool general, GroupPlan& gp) {
+  int gf = ps[0].f;  // the one format of a grouped launch, or -1 for mixed formats
+  for (int i = 1; i < n; ++i)
+    if (ps[i].f != gf) gf = -1;
+  const int64_t nsb = K / 256;
+  const int Wk = static_cast<int>((nsb + 7) / 8);
   const int cps = (Wk <= kMaxWarps / 2) ? h.ctas_per_sm : 1;  // CTAs per SM
+  int64_t V[kMaxGroup], U[kMaxGroup], rb1[kMaxGroup], rb2[kMaxGroup];
+  int64_t Vsum = 0;
+  double Bsum = 0;
+  bool any_pair = false;
+  for (int i = 0; i < n; ++i) {
+    stream_rows(ps[i].f, K, rb1[i], rb2[i]);
+    U[i] = ps[i].N;
+    V[i] = ps[i].pair ? 2 * ps[i].N : ps[i].N;  // virtual rows
+    Vsum += V[i];
+    Bsum += static_cast<double>(V[i]) * static_cast<double>(rb1[i] + rb2[i]);
+    any_pair = any_pair || ps[i].pair;
+  }
   // Split mode: a CTA takes one K-column of a row range with all its warps, so it stages only
   // that column of x; column sums meet in the workspace.  Fused mode: a CTA covers all
   // K-columns of its rows and adds the column sums in shared memory.
   // Two columns are faster fused (their x is small); from three on the split pays.
-  const bool split = Wk == 1 || (h.ksplit == 0 && Wk >= 3 && static_cast<double>(N) * Wk <= static_cast<double>(kWsFloats));
+  const bool split = Wk == 1 || (h.ksplit == 0 && Wk >= 3 && static_cast<double>(Vsum) * Wk <= static_cast<double>(kWsFloats));
   const int P = split ? kMaxWarps / cps : std::max(1, (kMaxWarps / cps) / Wk);
   const int warps = split ? P : P * Wk;
   // Under programmatic dependent launch a fused launch with few rows per warp (at most 16
   // with every slot filled) takes one CTA per SM: the next launch's CTAs then fit beside it
   // and fetch their first stages while this one finishes.
-  const bool short_pdl = h.pdl && !split && cps == 2 && N <= int64_t{16} * h.sms * cps * P;
+  const bool short_pdl = h.pdl && !split && cps == 2 && Vsum <= int64_t{16} * h.sms * cps * P;
   const int gps = h.grid_per_sm > 0 ? std::min(h.grid_per_sm, cps) : (short_pdl ? 1 : cps);
-  int64_t ranges, grid;
-  if (split) {
-    ranges = std::min<int64_t>(std::max(1, (h.sms * gps) / Wk), (N + P - 1) / P);
-    ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));
-    grid = ranges * Wk;
-  } else {
-    grid = std::min<int64_t>(int64_t{h.sms} * gps, (N + P - 1) / P);
-    if (Wk > 1) grid = std::max<int64_t>(grid, (N + (kRedBudget / (4 * Wk)) - 2) / (kRedBudget / (4 * Wk) - 1));
-    grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7fffffff));
-    ranges = grid;
+  const int64_t T = int64_t{h.sms} * gps;  // CTAs that fit at once
+  int64_t ranges[kMaxGroup], grid[kMaxGroup];
+  int red_rows[kMaxGroup] = {};
+  int64_t total_ranges = 0, total_grid = 0, ws_need = 0;
+  for (int i = 0; i < n; ++i) {
+    const double share = (static_cast<double>(V[i]) * static_cast<double>(rb1[i] + rb2[i])) / Bsum;
+    const int64_t units_max = (U[i] + P - 1) / P;  // at least one unit per row group
+    if (split) {
+      ranges[i] = std::min<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(static_cast<double>(T / Wk) * share)), units_max);
+      ranges[i] = std::max<int64_t>(1, ranges[i]);
+      grid[i] = ranges[i] * Wk;
+    } else {
+      grid[i] = std::min<int64_t>(std::max<int64_t>(1, static_cast<int64_t>(static_cast<double>(T) * share)), units_max);
+      if (Wk > 1) {  // the reduction buffer holds every row of a CTA
+        const int64_t per = (static_cast<int64_t>(kRedBudget / (4 * Wk)) - 1) / (ps[i].pair ? 2 : 1);
+        if (per < 1) return false;
+        grid[i] = std::max<int64_t>(grid[i], (U[i] + per - 1) / per);
+      }
+      grid[i] = std::max<int64_t>(1, grid[i]);
+      ranges[i] = grid[i];
+      red_rows[i] = static_cast<int>((ps[i].pair ? 2 : 1) * ((U[i] + grid[i] - 1) / grid[i]) + 1);
+    }
+    if (U[i] / ranges[i] >= 0x3ffffffe) return false;  // per-CTA row counts are 32-bit in the kernel
+    if (split && (Wk > 1 || ps[i].pair)) {  // sums through the workspace, one counter per range
+      total_ranges += ranges[i];
+      ws_need += V[i] * Wk;
+    }
+    total_grid += grid[i];
   }
-  if (N / ranges >= 0x7ffffffe) {  // per-CTA row counts are 32-bit in the kernel
-    rowwarp_plan(h, N, pl);
-    return QGEMV_OK;
-  }
-  const int red_rows = split ? 0 : static_cast<int>((N + grid - 1) / grid + 1);
+  if (total_ranges > kMaxRanges || ws_need > static_cast<int64_t>(kWsFloats)) return false;
+  if (total_grid > 0x7fffffff) return false;
   const int Kx = split ? static_cast<int>(std::min<int64_t>(K, 2048)) : static_cast<int>(K);
-  const int slice = slice_of(f);
-  // Defaults: 2 rows per stage, 4 stages; split launches (long K): 4 rows, 2 stages.
+  // Ring shape.  Defaults: 2 rows per stage, 4 stages; split launches (long K): 4 rows, 2
+  // stages; a one-CTA-per-SM launch of a two-per-SM layout: 4 rows, 3 stages.
   const bool long_k = split && Wk > 1;
-  const bool half = gps < cps;  // one CTA per SM of a two-per-SM layout
+  const bool half = gps < cps;
   int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : (long_k || half ? 4 : 2);
   int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : (long_k ? 2 : half ? 3 : 4);
+  const int Rmin = general ? 2 : 1;
+  if (R < Rmin) R = Rmin;
   const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
-  auto limit = [&](int d, int r) { return std::min(h.dyn_smem_max[f][r_index(r)][d_index(d)], cap); };
-  auto smem_of = [&](int d, int r) { return stream_smem(warps, d, r, slice, Wk, red_rows, Kx).total; };
-  while (smem_of(D, R) > limit(D, R) && (D > 2 || R > 1)) {
+  auto limit = [&](int d, int r) {
+    size_t m = cap;
+    for (int i = 0; i < n; ++i)
+      m = std::min(m, !general ? h.dyn_smem_max[ps[i].f][r_index(r)][d_index(d)]
+                      : gf >= 0 ? h.group1_smem_max[gf][r >= 4 ? 1 : 0][d_index(d)]
+                                : h.group_smem_max[r >= 4 ? 1 : 0][d_index(d)]);
+    return m;
+  };
+  auto smem_of = [&](int d, int r) {
+    size_t m = 0;
+    for (int i = 0; i < n; ++i) m = std::max(m, stream_smem(warps, d, r, slice_of(ps[i].f), Wk, red_rows[i], Kx).total);
+    return m;
+  };
+  while (smem_of(D, R) > limit(D, R) && (D > 2 || R > Rmin)) {
     if (D > 2)
       --D;
     else
       R >>= 1, D = 4;
   }
-  const size_t smem = smem_of(D, R);
-  if (smem > limit(D, R)) {
+  if (smem_of(D, R) > limit(D, R)) return false;
+  (void)any_pair;
+  gp.fmt = gf;
+  gp.grid = static_cast<int>(total_grid);
+  gp.threads = 32 * warps;
+  gp.R = R;
+  gp.D = D;
+  gp.smem = smem_of(D, R);
+  gp.ga.count = n;
+  int64_t cta = 0, rng = 0, ws_off = 0;
+  for (int i = 0; i < n; ++i) {
+    const Problem& q = ps[i];
+    StreamArgs& a = gp.ga.p[i];
+    a = StreamArgs{};
+    a.W = static_cast<const uint8_t*>(q.W);
+    a.W2 = (q.f == F_NVFP4) ? a.W + q.N * (K / 2) : nullptr;
+    a.WB = q.pair ? static_cast<const uint8_t*>(q.WB) : nullptr;
+    a.WB2 = (q.pair && q.f == F_NVFP4) ? a.WB + q.N * (K / 2) : nullptr;
+    a.y = q.y;
+    a.N = V[i];
+    a.rows_q = static_cast<int>(U[i] / ranges[i]);
+    a.rows_rem = static_cast<int>(U[i] % ranges[i]);
+    a.row_bytes = rb1[i];
+    a.row_bytes2 = rb2[i];
+    a.nsb = static_cast<int>(nsb);
+    a.Wk = Wk;
+    a.P = P;
+    a.red_rows = red_rows[i];
+    a.err = h.err;
+    a.spin_ns = h.spin_ns;
+    a.test_stall = i == 0 ? h.test_stall : 0;
+    // Under programmatic dependent launch, a launch that leaves room on each SM for the next
+    // one requests its first weight stages before waiting for the previous kernel (kernel
+    // mode 1); one that fills the SMs cannot overlap much, and takes x first (mode 2), so x is
+    // not queued behind its own weight stages.
+    a.pdl = !h.pdl ? 0 : (gps < cps ? 1 : 2);
+    a.split = split ? 1 : 0;
+    a.ws = h.ws + ws_off;
+    a.cnt = h.cnt + rng;
+    a.alpha = q.alpha;
+    a.beta = q.beta;
+    a.ydt = q.ydt;
+    a.pair = q.pair;
+    gp.ga.fmt[i] = q.f;
+    cta += grid[i];
+    gp.ga.cta_end[i] = static_cast<int>(cta);
+    if (split && (Wk > 1 || q.pair)) {
+      rng += ranges[i];
+      ws_off += V[i] * Wk;
+    }
+  }
+  return true;
+}
+
+// The single-matrix plan of qgemv_run / qgemv_describe.
+qgemv_status_t make_plan(const Handle& h, int f, int64_t N, int64_t K, Plan& pl) {
+  int64_t rb1 = 0, rb2 = 0;
+  if (!stream_rows(f, K, rb1, rb2) || h.force_path == 2) {
     rowwarp_plan(h, N, pl);
     return QGEMV_OK;
   }
-  StreamArgs& a = pl.sa;
-  a.N = N;
-  a.rows_q = static_cast<int>(N / ranges);
-  a.rows_rem = static_cast<int>(N % ranges);
-  a.row_bytes = rb1;
-  a.row_bytes2 = rb2;
-  a.nsb = static_cast<int>(nsb);
-  a.Wk = Wk;
-  a.P = P;
-  a.red_rows = red_rows;
-  a.err = h.err;
-  a.spin_ns = h.spin_ns;
-  a.test_stall = h.test_stall;
-  // Under programmatic dependent launch, a launch that leaves room on each SM for the next
-  // one requests its first weight stages before waiting for the previous kernel (kernel mode
-  // 1); one that fills the SMs cannot overlap much, and takes x first (mode 2), so x is not
-  // queued behind its own weight stages.
-  a.pdl = !h.pdl ? 0 : (gps < cps ? 1 : 2);
-  a.split = split ? 1 : 0;
-  a.ws = h.ws;
-  a.cnt = h.cnt;
+  Problem p;
+  p.f = f;
+  p.N = N;
+  GroupPlan gp;
+  if (!plan_stream(h, &p, 1, K, false, gp)) {
+    rowwarp_plan(h, N, pl);
+    return QGEMV_OK;
+  }
   pl.path = 1;
-  pl.grid = static_cast<int>(grid);
-  pl.threads = 32 * warps;
-  pl.R = R;
-  pl.D = D;
-  pl.smem = smem;
+  pl.sa = gp.ga.p[0];
+  pl.grid = gp.grid;
+  pl.threads = gp.threads;
+  pl.R = gp.R;
+  pl.D = gp.D;
+  pl.smem = gp.smem;
   return QGEMV_OK;
 }
 
@@ -334,6 +472,22 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
         return QGEMV_ERR_CUDA;
       }
     }
+  for (int f = -1; f <= 5; ++f)
+    for (int R : {2, 4})
+      for (int D : {2, 3, 4}) {
+        cudaFuncAttributes fa;
+        const void* fn = group_kernel_for(f, R, D);
+        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+          release();
+          return QGEMV_ERR_CUDA;
+        }
+        size_t& mx = f < 0 ? h->group_smem_max[R >= 4 ? 1 : 0][d_index(D)] : h->group1_smem_max[f][R >= 4 ? 1 : 0][d_index(D)];
+        mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
+          release();
+          return QGEMV_ERR_CUDA;
+        }
+      }
   *out = reinterpret_cast<qgemv_handle_t>(h);
   return QGEMV_OK;
 }
@@ -423,7 +577,7 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
   if (st != QGEMV_OK) return st;
   const uint8_t* Wb = static_cast<const uint8_t*>(W);
   if (pl.path == 2) {
-    RowArgs ra{Wb, static_cast<const uint16_t*>(x), y, N, K};
+    RowArgs ra{Wb, static_cast<const uint16_t*>(x), y, N, K, 1.f, 0.f, 0, 0, nullptr};
     launch_rowwarp_any(fmt, pl, ra, stream);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
   }
@@ -450,6 +604,97 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
     return QGEMV_ERR_CUDA;
   }
   return QGEMV_OK;
+}
+
+qgemv_status_t qgemv_run_group(qgemv_handle_t hh, const void* x, int64_t K, int count, const qgemv_problem_t* probs,
+                               cudaStream_t stream) {
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h || !probs || !x || count < 1 || count > kMaxGroup) return QGEMV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) & 15) return QGEMV_ERR_MISALIGNED;
+  Problem ps[kMaxGroup];
+  int nvfp4 = 0;
+  for (int i = 0; i < count; ++i) {
+    const qgemv_problem_t& q = probs[i];
+    const int f = static_cast<int>(q.fmt);
+    qgemv_status_t st = validate(h, f, q.packed_W, q.N, K);
+    if (st != QGEMV_OK) return st;
+    if (!q.y || q.swiglu < 0 || q.swiglu > 1 || q.out < QGEMV_OUT_F32 || q.out > QGEMV_OUT_BF16)
+      return QGEMV_ERR_INVALID_ARG;
+    if (q.swiglu && !q.packed_W_up) return QGEMV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q.y) | reinterpret_cast<uintptr_t>(q.packed_W_up)) & 15) return QGEMV_ERR_MISALIGNED;
+    nvfp4 += f == F_NVFP4;
+    ps[i].f = f;
+    ps[i].W = q.packed_W;
+    ps[i].WB = q.swiglu ? q.packed_W_up : nullptr;
+    ps[i].N = q.N;
+    ps[i].y = q.y;
+    ps[i].alpha = q.alpha;
+    ps[i].beta = q.beta;
+    ps[i].ydt = static_cast<int>(q.out);
+    ps[i].pair = q.swiglu;
+  }
+  if (nvfp4 != 0 && nvfp4 != count) return QGEMV_ERR_INVALID_ARG;  // one x: bf16 for NVFP4, fp16 otherwise
+  // Streaming-eligible matrices share one launch; the rest run warp per row.
+  Problem sp[kMaxGroup];
+  int ns = 0, nr = 0, rw[kMaxGroup];
+  for (int i = 0; i < count; ++i) {
+    int64_t rb1, rb2;
+    if (h->force_path != 2 && stream_rows(ps[i].f, K, rb1, rb2))
+      sp[ns++] = ps[i];
+    else
+      rw[nr++] = i;
+  }
+  GroupPlan gp;
+  if (ns > 0 && !plan_stream(*h, sp, ns, K, true, gp)) {
+    for (int i = 0; i < count; ++i) rw[i] = i;  // no ring shape fits: everything warp per row
+    nr = count;
+    ns = 0;
+  }
+  if (ns > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gp.grid, 1, 1);
+    cfg.blockDim = dim3(gp.threads, 1, 1);
+    cfg.dynamicSmemBytes = gp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (h->pdl) {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    for (int i = 0; i < ns; ++i) gp.ga.p[i].x = static_cast<const uint16_t*>(x);
+    void* args[] = {&gp.ga};
+    if (cudaLaunchKernelExC(&cfg, group_kernel_for(gp.fmt, gp.R, gp.D), args) != cudaSuccess) {
+      cudaGetLastError();
+      return QGEMV_ERR_CUDA;
+    }
+  }
+  for (int j = 0; j < nr; ++j) {
+    const Problem& q = ps[rw[j]];
+    Plan pl;
+    rowwarp_plan(*h, q.N, pl);
+    RowArgs ra{static_cast<const uint8_t*>(q.W), static_cast<const uint16_t*>(x), q.y, q.N, K, q.alpha, q.beta,
+               q.ydt, q.pair, static_cast<const uint8_t*>(q.WB)};
+    launch_rowwarp_any(q.f, pl, ra, stream);
+    if (cudaGetLastError() != cudaSuccess) return QGEMV_ERR_CUDA;
+  }
+  return QGEMV_OK;
+}
+
+qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x, const void* packed_W, int64_t N,
+                            int64_t K, float alpha, float beta, void* y, qgemv_out_t out, cudaStream_t stream) {
+  qgemv_problem_t p = {};
+  p.fmt = fmt;
+  p.packed_W = packed_W;
+  p.packed_W_up = nullptr;
+  p.N = N;
+  p.y = y;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.out = out;
+  p.swiglu = 0;
+  return qgemv_run_group(h, x, K, 1, &p, stream);
 }
 
 qgemv_status_t qgemv_unpack(qgemv_handle_t hh, qgemv_format_t fmt, const void* W, int64_t N, int64_t K, int8_t* codes,

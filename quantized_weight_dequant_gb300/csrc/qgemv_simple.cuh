@@ -11,6 +11,7 @@
 #include <cstdint>
 
 #include "qgemv_decode.cuh"
+#include "qgemv_epilogue.cuh"
 #include "qgemv_ptx.cuh"
 
 namespace qg {
@@ -19,8 +20,13 @@ namespace qg {
 struct RowArgs {
   const uint8_t* W;
   const uint16_t* x;
-  float* y;
+  void* y;
   int64_t N, K;
+  // Epilogue (see emit_out): y[n] = alpha r + beta y[n] as ydt; with pair = 1, r =
+  // silu(row n of W . x) * (row n of WB . x).  The plain GEMV uses 1, 0, fp32, no pair.
+  float alpha, beta;
+  int ydt, pair;
+  const uint8_t* WB;
 };
 
 __device__ __forceinline__ void kq_scale_min(const uint8_t* S, int g, int& s, int& m) {
@@ -105,37 +111,44 @@ template <> struct FmtGeom<F_Q80> { static constexpr int BW = 32, BB = 34; };
 template <> struct FmtGeom<F_TQ10> { static constexpr int BW = 256, BB = 54; };
 template <> struct FmtGeom<F_NVFP4> { static constexpr int BW = 16, BB = 8; };  // stream-1 bytes
 
+// Row n of matrix W (N x K) dotted with x by one warp; every lane returns the total.
+template <int F>
+__device__ float row_dot(const uint8_t* W, const RowArgs& a, int64_t n, int lane) {
+  constexpr int BW = FmtGeom<F>::BW, BB = FmtGeom<F>::BB;
+  const int64_t nb = a.K / BW;
+  float acc = 0.f;
+  for (int64_t b = lane; b < nb; b += 32) {
+    if constexpr (F == F_NVFP4) {
+      const uint8_t* nib = W + n * (a.K / 2) + b * 8;
+      const float s = fabsf(e4m3_f(W[a.N * (a.K / 2) + n * (a.K / 16) + b]));
+      float part = 0.f;
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t code = (nib[j >> 1] >> (4 * (j & 1))) & 15u;
+        part = fmaf(bf2f(a.x[b * 16 + j]), e2m1_f(code) * s, part);
+      }
+      acc += part;
+    } else {
+      const uint8_t* p = W + (n * nb + b) * BB;
+      for (int i = 0; i < BW; ++i) {
+        int code;
+        float scale, mn;
+        elem_code<F>(p, i, code, scale, mn);
+        const float w = fmaf(scale, static_cast<float>(code), -mn);
+        acc = fmaf(h2f(a.x[b * BW + i]), w, acc);
+      }
+    }
+  }
+  return warp_sum(acc);
+}
+
 template <int F>
 __global__ void __launch_bounds__(256) rowwarp_kernel(const RowArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  constexpr int BW = FmtGeom<F>::BW, BB = FmtGeom<F>::BB;
-  const int64_t nb = a.K / BW;
   for (int64_t n = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); n < a.N; n += warps) {
-    float acc = 0.f;
-    for (int64_t b = lane; b < nb; b += 32) {
-      if constexpr (F == F_NVFP4) {
-        const uint8_t* nib = a.W + n * (a.K / 2) + b * 8;
-        const float s = fabsf(e4m3_f(a.W[a.N * (a.K / 2) + n * (a.K / 16) + b]));
-        float part = 0.f;
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t code = (nib[j >> 1] >> (4 * (j & 1))) & 15u;
-          part = fmaf(bf2f(a.x[b * 16 + j]), e2m1_f(code) * s, part);
-        }
-        acc += part;
-      } else {
-        const uint8_t* p = a.W + (n * nb + b) * BB;
-        for (int i = 0; i < BW; ++i) {
-          int code;
-          float scale, mn;
-          elem_code<F>(p, i, code, scale, mn);
-          const float w = fmaf(scale, static_cast<float>(code), -mn);
-          acc = fmaf(h2f(a.x[b * BW + i]), w, acc);
-        }
-      }
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) a.y[n] = acc;
+    float r = row_dot<F>(a.W, a, n, lane);
+    if (a.pair) r = silu_f(r) * row_dot<F>(a.WB, a, n, lane);
+    if (lane == 0) emit_out(a.y, a.ydt, a.alpha, a.beta, n, r);
   }
 }
 

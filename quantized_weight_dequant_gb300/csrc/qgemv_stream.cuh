@@ -21,12 +21,17 @@
 //    (fixed point for the integer-code formats), then copied by each lane to registers.
 //  * Under programmatic dependent launch the first weight stages are requested before the
 //    wait for the previous kernel (weights are not written by it); x is read after it.
+//  * The body is shared by the single-matrix kernel (fp32 row sums stored as they are) and
+//    the grouped kernel (several matrices of possibly different formats sharing x, one per
+//    CTA range, with the general epilogue out = alpha r + beta out in fp32/fp16/bf16, and
+//    the SwiGLU pairing of a gate and an up matrix).
 #pragma once
 #include <cuda_fp16.h>
 
 #include <cstdint>
 
 #include "qgemv_decode.cuh"
+#include "qgemv_epilogue.cuh"
 #include "qgemv_ptx.cuh"
 
 // Optional tracing hooks for timeline studies: empty unless defined before this header.
@@ -45,9 +50,10 @@ struct StreamArgs {
   const uint8_t* W;     // stream 1: rows of packed blocks / NVFP4 nibbles
   const uint8_t* W2;    // stream 2: NVFP4 scales (null otherwise)
   const uint16_t* x;    // activations (fp16, bf16 for NVFP4)
-  float* y;
-  int64_t N;
-  int rows_q, rows_rem; // N = gridDim.x * rows_q + rows_rem: CTA b has rows_q (+1 if b < rows_rem)
+  void* y;              // fp32 row sums (single-matrix kernel); grouped kernel: see ydt
+  int64_t N;            // rows (virtual rows, 2 per output, with pair = 1)
+  int rows_q, rows_rem; // units (rows; pairs with pair = 1) = ranges * rows_q + rows_rem:
+                        // range b has rows_q units (+1 if b < rows_rem)
   int64_t row_bytes, row_bytes2;  // bytes per row of stream 1 / 2 (multiples of 16)
   int nsb;              // superblocks per row
   int Wk;               // K-columns (warps per row group) = ceil(nsb / 8)
@@ -64,7 +70,40 @@ struct StreamArgs {
   int split;
   float* ws;
   int* cnt;
+  // Epilogue of the grouped kernel: out = alpha * r + beta * out (out is not read when
+  // beta == 0), stored as ydt (0 fp32, 1 fp16, 2 bf16, round to nearest even).  r is the row
+  // sum; with pair = 1 (SwiGLU) virtual row 2n is row n of the gate matrix (W, W2) and
+  // virtual row 2n + 1 row n of the up matrix (WB, WB2), and r = silu(gate sum) * up sum.
+  float alpha, beta;
+  int ydt;
+  int pair;
+  const uint8_t* WB;
+  const uint8_t* WB2;
 };
+
+// Grouped launch: CTAs [cta_end[i-1], cta_end[i]) run matrix i, of format fmt[i].
+constexpr int kMaxGroup = 8;
+struct GroupArgs {
+  int count;
+  int cta_end[kMaxGroup];
+  int fmt[kMaxGroup];
+  StreamArgs p[kMaxGroup];
+};
+
+__device__ __forceinline__ void emit(const StreamArgs& a, int64_t n, float r) {
+  emit_out(a.y, a.ydt, a.alpha, a.beta, n, r);
+}
+
+// The Wk column sums of virtual row `row` (split mode), added in column order.
+__device__ __forceinline__ float column_sum(const StreamArgs& a, int64_t row) {
+  float v[16];  // all column sums of the row in flight at once (Wk <= 16)
+#pragma unroll
+  for (int w = 0; w < 16; ++w) v[w] = w < a.Wk ? __ldcg(a.ws + w * a.N + row) : 0.f;
+  float s = v[0];
+#pragma unroll
+  for (int w = 1; w < 16; ++w) s += v[w];  // the zero padding adds nothing
+  return s;
+}
 
 template <class Dec>
 __host__ __device__ constexpr int slice_bytes() {
@@ -128,10 +167,11 @@ __device__ __forceinline__ float reduce_rows(const float (&v)[R], int lane) {
   return t;
 }
 
-template <class Dec, int R, int D>
-__global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
+// One CTA's work: CTA `cta` of the launch (or of its matrix in a grouped launch).  GEN
+// enables the grouped kernel's epilogue and pairing; without it the fp32 row sums are stored.
+template <class Dec, int R, int D, bool GEN>
+__device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, uint8_t* smem) {
   QG_TRACE(0);
-  extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = Dec::kSB, SB2 = Dec::kSB2, SLICE = slice_bytes<Dec>();
   constexpr int STAGE = R * SLICE;
   constexpr int J1 = (8 * SB / 16 + 31) / 32, J2 = (8 * SB2 / 16 + 31) / 32;  // copies per lane per row
@@ -141,16 +181,30 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   // Fused mode: warp = (row group p, K-column wk) over all Wk columns of the CTA's rows.
   // Split mode: every warp of the CTA is on K-column blockIdx.x % Wk.
   const int p = a.split ? warp : warp / a.Wk;
-  const int wk = a.split ? static_cast<int>(blockIdx.x % a.Wk) : warp % a.Wk;
+  const unsigned ucta = GEN ? static_cast<unsigned>(cta) : blockIdx.x, uWk = static_cast<unsigned>(a.Wk);
+  const int wk = a.split ? static_cast<int>(ucta % uWk) : warp % a.Wk;
   const int kc0 = a.split ? wk : 0, kc1 = a.split ? wk + 1 : a.Wk;  // K-columns this CTA reads
 
-  // Contiguous row ranges: range b, then row group p within it (no 64-bit division).
-  const int b = a.split ? static_cast<int>(blockIdx.x / a.Wk) : static_cast<int>(blockIdx.x);
-  const int64_t r_lo = static_cast<int64_t>(b) * a.rows_q + min(b, a.rows_rem);
-  const int ncta = a.rows_q + (b < a.rows_rem ? 1 : 0);
-  const int pq = ncta / a.P, prem = ncta % a.P;
-  const int64_t p_lo = r_lo + p * pq + min(p, prem);
-  const int nrows = pq + (p < prem ? 1 : 0);
+  // Contiguous row ranges: range b, then row group p within it (no 64-bit division), in
+  // units of u rows (a gate/up pair of virtual rows with pair = 1).
+  const bool pair = GEN && R >= 2 && a.pair;
+  const int b = a.split ? static_cast<int>(ucta / uWk) : static_cast<int>(ucta);
+  int64_t r_lo, p_lo;
+  int ncta, nrows;
+  if (pair) {
+    r_lo = 2 * (static_cast<int64_t>(b) * a.rows_q + min(b, a.rows_rem));
+    const int ncu = a.rows_q + (b < a.rows_rem ? 1 : 0);
+    const int pq = ncu / a.P, prem = ncu % a.P;
+    ncta = 2 * ncu;
+    p_lo = r_lo + 2 * (p * pq + min(p, prem));
+    nrows = 2 * (pq + (p < prem ? 1 : 0));
+  } else {
+    r_lo = static_cast<int64_t>(b) * a.rows_q + min(b, a.rows_rem);
+    ncta = a.rows_q + (b < a.rows_rem ? 1 : 0);
+    const int pq = ncta / a.P, prem = ncta % a.P;
+    p_lo = r_lo + p * pq + min(p, prem);
+    nrows = pq + (p < prem ? 1 : 0);
+  }
   const int ncols = min(8, a.nsb - 8 * wk);
   const int col = lane >> 2;
   const bool active = col < ncols;
@@ -165,7 +219,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   uint64_t* never_bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
   pdl_launch_dependents();  // the next kernel may start copying its weights right away
-  if (a.test_stall && blockIdx.x == 0 && warp == 0) {
+  if (a.test_stall && cta == 0 && warp == 0) {
     if (lane == 0) {
       mbar_init(smem_u32(never_bar), 1);
       fence_mbar_init();
@@ -183,10 +237,25 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   for (int j = 0; j < J2; ++j) ok2[j] = lane + 32 * j < n2;
   // Rows of a stage are requested in order through running pointers; row bytes fit in 32 bits.
   const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
+  // Pairs: a warp streams the gate rows of its outputs (from gi), then their up rows (from
+  // gb), one matrix at a time; both sums go to the workspace / reduction buffer, where the
+  // epilogue combines them.
   const uint8_t* gi1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
   const uint8_t* gi2 = (SB2 > 0) ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane : a.W;
+  const uint8_t* gb1 = a.W;
+  const uint8_t* gb2 = a.W;
+  if (pair) {
+    const int64_t wrow = p_lo / 2;
+    gi1 = a.W + wrow * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
+    gb1 = a.WB + wrow * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
+    if (SB2 > 0) {
+      gi2 = a.W2 + wrow * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane;
+      gb2 = a.WB2 + wrow * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane;
+    }
+  }
   const uint32_t ring_sa = smem_u32(ring), ring_end = ring_sa + D * STAGE;
   const int nst = (nrows + R - 1) / R, nfull = nrows / R, tail = nrows - nfull * R;
+  const int np = nrows / 2;  // pairs: outputs of this warp
 
   // This lane's copies of one row slice: to shared address d, from row pointers s1 / s2.
   auto copy_row = [&](uint32_t d, const uint8_t* s1, const uint8_t* s2) {
@@ -210,6 +279,31 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   // decoded and dropped).
   auto issue = [&](int st, uint32_t slot_sa) {
     const uint32_t d = slot_sa + 16 * lane;
+    if constexpr (GEN && R >= 2) {
+      if (pair) {  // position q: gate row q (q < np) or up row q - np
+        const int q0 = st * R;
+        if (q0 + R <= np || (q0 >= np && q0 + R <= nrows)) {  // a whole stage of one matrix
+          const bool up = q0 >= np;
+          const int64_t j = up ? q0 - np : q0;
+          const uint8_t* s1 = (up ? gb1 : gi1) + j * rb1;
+          const uint8_t* s2 = (up ? gb2 : gi2) + j * rb2;
+#pragma unroll
+          for (int r = 0; r < R; ++r) copy_row(d + r * SLICE, s1 + r * rb1, s2 + r * rb2);
+        } else {  // the stage that crosses from gate to up rows, or the short last one
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int q = q0 + r;
+            if (q < nrows) {
+              const bool up = q >= np;
+              const int64_t j = up ? q - np : q;
+              copy_row(d + r * SLICE, (up ? gb1 : gi1) + j * rb1, (up ? gb2 : gi2) + j * rb2);
+            }
+          }
+        }
+        cp_async_commit();
+        return;
+      }
+    }
     if (st < nfull) {
 #pragma unroll
       for (int r = 0; r < R; ++r) copy_row(d + r * SLICE, gi1 + r * rb1, gi2 + r * rb2);
@@ -267,7 +361,7 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
 
   // Where row sums go: y (one K-column), the workspace (split mode) or the CTA's reduction
   // buffer (fused mode, stride Wk).
-  float* const out = a.Wk == 1 ? a.y + p_lo
+  float* const out = (a.Wk == 1 && !pair) ? static_cast<float*>(a.y) + p_lo
                      : a.split ? a.ws + wk * a.N + p_lo
                                : red + static_cast<int>(p_lo - r_lo) * a.Wk + wk;
   const int ostride = (a.Wk == 1 || a.split) ? 1 : a.Wk;
@@ -294,20 +388,40 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) v[r] = active ? v[r] : 0.f;
     const float sum = reduce_rows<R>(v, lane);
-    if (writer && st * R + lane / LPR < nrows) *optr = sum;
-    optr += R * ostride;
+    if (pair) {  // virtual row 2j (gate) or 2j + 1 (up) of the warp's output j
+      const int q = st * R + lane / LPR;
+      if (writer && q < nrows) out[(q < np ? 2 * q : 2 * (q - np) + 1) * ostride] = sum;
+    } else if (GEN && a.Wk == 1) {  // final sums: the epilogue
+      const int rr = st * R + lane / LPR;
+      if (writer && rr < nrows) emit(a, p_lo + rr, sum);
+    } else {
+      if (writer && st * R + lane / LPR < nrows) *optr = sum;
+      optr += R * ostride;
+    }
   }
   cp_async_wait<0>();
   QG_TRACE(4);
 
   if (a.Wk > 1 && !a.split) {
     __syncthreads();
-    for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
-      float s = 0.f;
-      for (int w = 0; w < a.Wk; ++w) s += red[i * a.Wk + w];
-      a.y[r_lo + i] = s;
+    if (pair) {
+      for (int i = threadIdx.x; i < ncta / 2; i += blockDim.x) {
+        float g = 0.f, up = 0.f;
+        for (int w = 0; w < a.Wk; ++w) g += red[(2 * i) * a.Wk + w];
+        for (int w = 0; w < a.Wk; ++w) up += red[(2 * i + 1) * a.Wk + w];
+        emit(a, (r_lo >> 1) + i, silu_f(g) * up);
+      }
+    } else {
+      for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < a.Wk; ++w) s += red[i * a.Wk + w];
+        if (GEN)
+          emit(a, r_lo + i, s);
+        else
+          static_cast<float*>(a.y)[r_lo + i] = s;
+      }
     }
-  } else if (a.Wk > 1) {
+  } else if (a.Wk > 1 || pair) {
     // Publish this CTA's column sums, then count the CTA in; the last of the Wk CTAs of the
     // row range adds the Wk column sums of each row in column order and resets the count.
     __shared__ int last;
@@ -321,20 +435,70 @@ __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
     }
     __syncthreads();
     if (last) {
-      for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
-        float v[16];  // all column sums of the row in flight at once (Wk <= 16)
-#pragma unroll
-        for (int w = 0; w < 16; ++w) v[w] = w < a.Wk ? __ldcg(a.ws + w * a.N + r_lo + i) : 0.f;
-        float s = v[0];
-#pragma unroll
-        for (int w = 1; w < 16; ++w) s += v[w];  // column order; the zero padding adds nothing
-        a.y[r_lo + i] = s;
+      if (pair) {
+        for (int i = threadIdx.x; i < ncta / 2; i += blockDim.x)
+          emit(a, (r_lo >> 1) + i, silu_f(column_sum(a, r_lo + 2 * i)) * column_sum(a, r_lo + 2 * i + 1));
+      } else {
+        for (int i = threadIdx.x; i < ncta; i += blockDim.x) {
+          const float s = column_sum(a, r_lo + i);
+          if (GEN)
+            emit(a, r_lo + i, s);
+          else
+            static_cast<float*>(a.y)[r_lo + i] = s;
+        }
       }
       if (threadIdx.x == 0) a.cnt[b] = 0;
     }
   }
   QG_TRACE(5);
   QG_TRACE_END();
+}
+
+// Single matrix: fp32 row sums.
+template <class Dec, int R, int D>
+__global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  stream_body<Dec, R, D, false>(a, static_cast<int>(blockIdx.x), smem);
+}
+
+// Grouped launch of matrices of one format (the common case: a smaller kernel than the
+// mixed-format one below, whose six decoders crowd the instruction cache).
+template <class Dec, int R, int D>
+__global__ void __launch_bounds__(512, 1) group_kernel_1(const __grid_constant__ GroupArgs g) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int i = 0;
+  while (i + 1 < g.count && static_cast<int>(blockIdx.x) >= g.cta_end[i]) ++i;
+  stream_body<Dec, R, D, true>(g.p[i], static_cast<int>(blockIdx.x) - (i > 0 ? g.cta_end[i - 1] : 0), smem);
+}
+
+// Grouped launch: up to kMaxGroup matrices (any formats, one x) with the general epilogue.
+template <int R, int D>
+__global__ void __launch_bounds__(512, 1) group_kernel(const __grid_constant__ GroupArgs g) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int i = 0;
+  while (i + 1 < g.count && static_cast<int>(blockIdx.x) >= g.cta_end[i]) ++i;
+  const int cta = static_cast<int>(blockIdx.x) - (i > 0 ? g.cta_end[i - 1] : 0);
+  const StreamArgs& a = g.p[i];
+  switch (g.fmt[i]) {
+    case F_Q4K: stream_body<DecQ4K, R, D, true>(a, cta, smem); break;
+    case F_Q5K: stream_body<DecQ5K, R, D, true>(a, cta, smem); break;
+    case F_Q6K: stream_body<DecQ6K, R, D, true>(a, cta, smem); break;
+    case F_Q80: stream_body<DecQ80, R, D, true>(a, cta, smem); break;
+    case F_TQ10: stream_body<DecTQ10, R, D, true>(a, cta, smem); break;
+    case F_NVFP4: stream_body<DecNVFP4, R, D, true>(a, cta, smem); break;
+  }
+}
+
+// One-format grouped kernels of one decoder: R in {2, 4}, D in {2, 3, 4}.
+template <class Dec>
+const void* group_kernel_1_table(int R, int D) {
+  const int di = D >= 4 ? 2 : D >= 3 ? 1 : 0;
+  static const void* const t[2][3] = {
+      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 2>), reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 3>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 4>)},
+      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 2>), reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 3>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 4>)}};
+  return t[R >= 4 ? 1 : 0][di];
 }
 
 // Kernel table of one decoder: R in {1, 2, 4} rows per stage, D in {2, 3, 4} ring stages.

@@ -20,10 +20,19 @@ STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED_F
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_FORMAT, ERR_BAD_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
     ERR_NO_DEVICE, ERR_TOO_LARGE = range(10)
 NOALLOC_MAX_COLUMN_SUMS = 262144  # QGEMV_NOALLOC_MAX_COLUMN_SUMS
+OUT_F32, OUT_F16, OUT_BF16 = 0, 1, 2
+MAX_GROUP = 8  # QGEMV_MAX_GROUP
+
+
+class Problem(ctypes.Structure):
+    """qgemv_problem_t: one matrix of run_group."""
+    _fields_ = [("fmt", ctypes.c_int), ("packed_W", ctypes.c_void_p), ("packed_W_up", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("y", ctypes.c_void_p), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float), ("out", ctypes.c_int), ("swiglu", ctypes.c_int)]
 
 EXPORTS = ["qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
            "qgemv_status_string", "qgemv_packed_bytes", "qgemv_group_size", "qgemv_set_option",
-           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc"]
+           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc", "qgemv_run_group", "qgemv_run_ex"]
 
 _lib = None
 
@@ -56,8 +65,12 @@ def lib() -> ctypes.CDLL:
         L.qgemv_describe.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_char_p, ctypes.c_size_t]
         L.qgemv_build_marker.restype = ctypes.c_char_p
         L.qgemv_run_noalloc.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp, vp]
+        L.qgemv_run_group.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.POINTER(Problem), vp]
+        L.qgemv_run_ex.argtypes = [vp, ctypes.c_int, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, vp,
+                                   ctypes.c_int, vp]
         for name in ("qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
-                     "qgemv_set_option", "qgemv_describe", "qgemv_run_noalloc"):
+                     "qgemv_set_option", "qgemv_describe", "qgemv_run_noalloc", "qgemv_run_group",
+                     "qgemv_run_ex"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -148,6 +161,30 @@ def run_noalloc(fmt: int, x, packed_W, N: int, K: int, y, stream=None, check: bo
     st = lib().qgemv_run_noalloc(fmt, _ptr(x), _ptr(packed_W), N, K, _ptr(y), _stream(stream))
     if check:
         _check(st, "qgemv_run_noalloc")
+    return st
+
+
+def run_ex(h: Handle, fmt: int, x, packed_W, N: int, K: int, y, alpha: float = 1.0, beta: float = 0.0,
+           out: int = OUT_F32, stream=None, check: bool = True) -> int:
+    """y = alpha * x . dequant(W)^T + beta * y, y of type `out` (OUT_F32 / OUT_F16 / OUT_BF16)."""
+    st = lib().qgemv_run_ex(h.ptr, fmt, _ptr(x), _ptr(packed_W), N, K, alpha, beta, _ptr(y), out,
+                            _stream(stream))
+    if check:
+        _check(st, "qgemv_run_ex")
+    return st
+
+
+def problem(fmt: int, packed_W, N: int, y, packed_W_up=None, alpha: float = 1.0, beta: float = 0.0,
+            out: int = OUT_F32, swiglu: bool = False) -> Problem:
+    return Problem(fmt, _ptr(packed_W), _ptr(packed_W_up), N, _ptr(y), alpha, beta, out, int(swiglu))
+
+
+def run_group(h: Handle, x, K: int, problems, stream=None, check: bool = True) -> int:
+    """GEMVs sharing x (a list of `problem(...)` entries, at most MAX_GROUP), one launch."""
+    arr = (Problem * max(1, len(problems)))(*problems)
+    st = lib().qgemv_run_group(h.ptr, _ptr(x), K, len(problems), arr, _stream(stream))
+    if check:
+        _check(st, "qgemv_run_group")
     return st
 
 
