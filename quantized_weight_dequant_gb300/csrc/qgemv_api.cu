@@ -36,7 +36,7 @@ struct Handle {
   int grid_per_sm = 0;  // CTAs launched per SM (0: as many as fit, ctas_per_sm)
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
-  size_t group1_smem_max[6][2][3] = {};  // one-format grouped kernels [format][R 2/4][D 2/3/4]
+  size_t group1_smem_max[6][2][2][3] = {};  // one-format grouped kernels [format][pairs][R 2/4][D 2/3/4]
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -110,6 +110,7 @@ struct Plan {
 struct GroupPlan {
   GroupArgs ga{};
   int fmt = -1;  // the one format of the launch, or -1 for mixed formats
+  bool pairs = false;  // one format, every matrix a SwiGLU pair
   int grid = 0, threads = 0, R = 2, D = 4;
   size_t smem = 0;
 };
@@ -132,6 +133,12 @@ const void* group_kernel_q6k(int R, int D);
 const void* group_kernel_q80(int R, int D);
 const void* group_kernel_tq10(int R, int D);
 const void* group_kernel_nvfp4(int R, int D);
+const void* group_kernel_pair_q4k(int R, int D);
+const void* group_kernel_pair_q5k(int R, int D);
+const void* group_kernel_pair_q6k(int R, int D);
+const void* group_kernel_pair_q80(int R, int D);
+const void* group_kernel_pair_tq10(int R, int D);
+const void* group_kernel_pair_nvfp4(int R, int D);
 }  // namespace qg
 
 namespace {
@@ -148,9 +155,19 @@ const void* stream_kernel_for(int f, int R, int D) {
   return nullptr;
 }
 
-// Grouped kernel for ring shape (R, D): the one-format kernel of format f, or (f < 0) the
-// mixed-format one.
-const void* group_kernel_for(int f, int R, int D) {
+// Grouped kernel for ring shape (R, D): the one-format kernel of format f (with the SwiGLU
+// pairing compiled in when every matrix is a pair), or (f < 0) the mixed-format one.
+const void* group_kernel_for(int f, int R, int D, bool pairs = false) {
+  if (pairs) {
+    switch (f) {
+      case F_Q4K: return group_kernel_pair_q4k(R, D);
+      case F_Q5K: return group_kernel_pair_q5k(R, D);
+      case F_Q6K: return group_kernel_pair_q6k(R, D);
+      case F_Q80: return group_kernel_pair_q80(R, D);
+      case F_TQ10: return group_kernel_pair_tq10(R, D);
+      case F_NVFP4: return group_kernel_pair_nvfp4(R, D);
+    }
+  }
   switch (f) {
     case F_Q4K: return group_kernel_q4k(R, D);
     case F_Q5K: return group_kernel_q5k(R, D);
@@ -191,8 +208,12 @@ bool stream_rows(int f, int64_t K, int64_t& rb1, int64_t& rb2) {
 // are R in {2, 4}.  Returns false when no ring shape fits (the caller falls back).
 bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool general, GroupPlan& gp) {
   int gf = ps[0].f;  // the one format of a grouped launch, or -1 for mixed formats
-  for (int i = 1; i < n; ++i)
+  bool all_pairs = true;
+  for (int i = 0; i < n; ++i) {
     if (ps[i].f != gf) gf = -1;
+    all_pairs = all_pairs && ps[i].pair;
+  }
+  const bool pairs = gf >= 0 && all_pairs;
   const int64_t nsb = K / 256;
   const int Wk = static_cast<int>((nsb + 7) / 8);
   const int cps = (Wk <= kMaxWarps / 2) ? h.ctas_per_sm : 1;  // CTAs per SM
@@ -265,7 +286,7 @@ bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool gene
     size_t m = cap;
     for (int i = 0; i < n; ++i)
       m = std::min(m, !general ? h.dyn_smem_max[ps[i].f][r_index(r)][d_index(d)]
-                      : gf >= 0 ? h.group1_smem_max[gf][r >= 4 ? 1 : 0][d_index(d)]
+                      : gf >= 0 ? h.group1_smem_max[gf][pairs ? 1 : 0][r >= 4 ? 1 : 0][d_index(d)]
                                 : h.group_smem_max[r >= 4 ? 1 : 0][d_index(d)]);
     return m;
   };
@@ -283,6 +304,7 @@ bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool gene
   if (smem_of(D, R) > limit(D, R)) return false;
   (void)any_pair;
   gp.fmt = gf;
+  gp.pairs = pairs;
   gp.grid = static_cast<int>(total_grid);
   gp.threads = 32 * warps;
   gp.R = R;
@@ -473,21 +495,23 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
       }
     }
   for (int f = -1; f <= 5; ++f)
-    for (int R : {2, 4})
-      for (int D : {2, 3, 4}) {
-        cudaFuncAttributes fa;
-        const void* fn = group_kernel_for(f, R, D);
-        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
-          release();
-          return QGEMV_ERR_CUDA;
+    for (int pr = 0; pr < (f < 0 ? 1 : 2); ++pr)
+      for (int R : {2, 4})
+        for (int D : {2, 3, 4}) {
+          cudaFuncAttributes fa;
+          const void* fn = group_kernel_for(f, R, D, pr == 1);
+          if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+            release();
+            return QGEMV_ERR_CUDA;
+          }
+          size_t& mx = f < 0 ? h->group_smem_max[R >= 4 ? 1 : 0][d_index(D)]
+                             : h->group1_smem_max[f][pr][R >= 4 ? 1 : 0][d_index(D)];
+          mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
+          if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
+            release();
+            return QGEMV_ERR_CUDA;
+          }
         }
-        size_t& mx = f < 0 ? h->group_smem_max[R >= 4 ? 1 : 0][d_index(D)] : h->group1_smem_max[f][R >= 4 ? 1 : 0][d_index(D)];
-        mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
-          release();
-          return QGEMV_ERR_CUDA;
-        }
-      }
   *out = reinterpret_cast<qgemv_handle_t>(h);
   return QGEMV_OK;
 }
@@ -665,7 +689,7 @@ qgemv_status_t qgemv_run_group(qgemv_handle_t hh, const void* x, int64_t K, int 
     }
     for (int i = 0; i < ns; ++i) gp.ga.p[i].x = static_cast<const uint16_t*>(x);
     void* args[] = {&gp.ga};
-    if (cudaLaunchKernelExC(&cfg, group_kernel_for(gp.fmt, gp.R, gp.D), args) != cudaSuccess) {
+    if (cudaLaunchKernelExC(&cfg, group_kernel_for(gp.fmt, gp.R, gp.D, gp.pairs), args) != cudaSuccess) {
       cudaGetLastError();
       return QGEMV_ERR_CUDA;
     }

@@ -167,9 +167,10 @@ __device__ __forceinline__ float reduce_rows(const float (&v)[R], int lane) {
   return t;
 }
 
-// One CTA's work: CTA `cta` of the launch (or of its matrix in a grouped launch).  GEN
-// enables the grouped kernel's epilogue and pairing; without it the fp32 row sums are stored.
-template <class Dec, int R, int D, bool GEN>
+// One CTA's work: CTA `cta` of the launch (or of its matrix in a grouped launch).  MODE 0:
+// the fp32 row sums are stored; 1: the grouped kernel's epilogue, pairs decided at run time
+// (a.pair); 2: the same for launches whose matrices are all SwiGLU pairs.
+template <class Dec, int R, int D, int MODE>
 __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, uint8_t* smem) {
   QG_TRACE(0);
   constexpr int SB = Dec::kSB, SB2 = Dec::kSB2, SLICE = slice_bytes<Dec>();
@@ -181,13 +182,14 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   // Fused mode: warp = (row group p, K-column wk) over all Wk columns of the CTA's rows.
   // Split mode: every warp of the CTA is on K-column blockIdx.x % Wk.
   const int p = a.split ? warp : warp / a.Wk;
+  constexpr bool GEN = MODE > 0;
   const unsigned ucta = GEN ? static_cast<unsigned>(cta) : blockIdx.x, uWk = static_cast<unsigned>(a.Wk);
   const int wk = a.split ? static_cast<int>(ucta % uWk) : warp % a.Wk;
   const int kc0 = a.split ? wk : 0, kc1 = a.split ? wk + 1 : a.Wk;  // K-columns this CTA reads
 
   // Contiguous row ranges: range b, then row group p within it (no 64-bit division), in
   // units of u rows (a gate/up pair of virtual rows with pair = 1).
-  const bool pair = GEN && R >= 2 && a.pair;
+  const bool pair = MODE == 2 || (MODE == 1 && R >= 2 && a.pair);
   const int b = a.split ? static_cast<int>(ucta / uWk) : static_cast<int>(ucta);
   int64_t r_lo, p_lo;
   int ncta, nrows;
@@ -458,17 +460,18 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
 template <class Dec, int R, int D>
 __global__ void __launch_bounds__(512, 1) stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  stream_body<Dec, R, D, false>(a, static_cast<int>(blockIdx.x), smem);
+  stream_body<Dec, R, D, 0>(a, static_cast<int>(blockIdx.x), smem);
 }
 
 // Grouped launch of matrices of one format (the common case: a smaller kernel than the
 // mixed-format one below, whose six decoders crowd the instruction cache).
-template <class Dec, int R, int D>
+// PAIRS: every matrix of the launch is a SwiGLU pair (the pairing compiled in).
+template <class Dec, int R, int D, bool PAIRS>
 __global__ void __launch_bounds__(512, 1) group_kernel_1(const __grid_constant__ GroupArgs g) {
   extern __shared__ __align__(128) uint8_t smem[];
   int i = 0;
   while (i + 1 < g.count && static_cast<int>(blockIdx.x) >= g.cta_end[i]) ++i;
-  stream_body<Dec, R, D, true>(g.p[i], static_cast<int>(blockIdx.x) - (i > 0 ? g.cta_end[i - 1] : 0), smem);
+  stream_body<Dec, R, D, PAIRS ? 2 : 1>(g.p[i], static_cast<int>(blockIdx.x) - (i > 0 ? g.cta_end[i - 1] : 0), smem);
 }
 
 // Grouped launch: up to kMaxGroup matrices (any formats, one x) with the general epilogue.
@@ -480,24 +483,27 @@ __global__ void __launch_bounds__(512, 1) group_kernel(const __grid_constant__ G
   const int cta = static_cast<int>(blockIdx.x) - (i > 0 ? g.cta_end[i - 1] : 0);
   const StreamArgs& a = g.p[i];
   switch (g.fmt[i]) {
-    case F_Q4K: stream_body<DecQ4K, R, D, true>(a, cta, smem); break;
-    case F_Q5K: stream_body<DecQ5K, R, D, true>(a, cta, smem); break;
-    case F_Q6K: stream_body<DecQ6K, R, D, true>(a, cta, smem); break;
-    case F_Q80: stream_body<DecQ80, R, D, true>(a, cta, smem); break;
-    case F_TQ10: stream_body<DecTQ10, R, D, true>(a, cta, smem); break;
-    case F_NVFP4: stream_body<DecNVFP4, R, D, true>(a, cta, smem); break;
+    case F_Q4K: stream_body<DecQ4K, R, D, 1>(a, cta, smem); break;
+    case F_Q5K: stream_body<DecQ5K, R, D, 1>(a, cta, smem); break;
+    case F_Q6K: stream_body<DecQ6K, R, D, 1>(a, cta, smem); break;
+    case F_Q80: stream_body<DecQ80, R, D, 1>(a, cta, smem); break;
+    case F_TQ10: stream_body<DecTQ10, R, D, 1>(a, cta, smem); break;
+    case F_NVFP4: stream_body<DecNVFP4, R, D, 1>(a, cta, smem); break;
   }
 }
 
-// One-format grouped kernels of one decoder: R in {2, 4}, D in {2, 3, 4}.
-template <class Dec>
+// One-format grouped kernels of one decoder: R in {2, 4}, D in {2, 3, 4}, pairs compiled in
+// or not.
+template <class Dec, bool PAIRS>
 const void* group_kernel_1_table(int R, int D) {
   const int di = D >= 4 ? 2 : D >= 3 ? 1 : 0;
   static const void* const t[2][3] = {
-      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 2>), reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 3>),
-       reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 4>)},
-      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 2>), reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 3>),
-       reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 4>)}};
+      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 2, PAIRS>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 3, PAIRS>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 2, 4, PAIRS>)},
+      {reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 2, PAIRS>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 3, PAIRS>),
+       reinterpret_cast<const void*>(&group_kernel_1<Dec, 4, 4, PAIRS>)}};
   return t[R >= 4 ? 1 : 0][di];
 }
 
