@@ -245,6 +245,25 @@ qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x,
                             int64_t N, int64_t K, float alpha, float beta, void* y, qgemv_out_t out,
                             cudaStream_t stream);
 
+/* ---------------------------------------------------------------- small batches
+ * Y = X . dequant(W)^T for M = 1..QGEMV_MAX_BATCH activation vectors at once (the general
+ * GEMV of the Q4_K page, "What is a GEMV", with x of shape (M, K) instead of (1, K)): every
+ * packed weight is read and decoded once and serves all M vectors.  Q4_K and NVFP4 with
+ * K a multiple of 256 use the tensor cores' mma.sync path (decoded weights go straight into
+ * the B fragments; the M vectors fill the A operand), as long as M * N * ceil(K / 2048) fits
+ * the handle's workspace (4 Mi column sums); other formats and shapes run the single-vector
+ * path once per vector. */
+#define QGEMV_MAX_BATCH 8
+
+/* x: device, M rows of K 16-bit values (fp16; bf16 for NVFP4), row-major, 16-byte aligned.
+ * y: device, M rows of N fp32 values, row-major (y[m * N + n]), 16-byte aligned.
+ * packed_W, N, K: as qgemv_run.  1 <= M <= QGEMV_MAX_BATCH, else QGEMV_ERR_INVALID_ARG.
+ * Validation, asynchrony, workspace use and determinism as qgemv_run.  Each output obeys the
+ * GEMV tolerance of its own vector. */
+qgemv_status_t qgemv_run_batch(qgemv_handle_t h, qgemv_format_t fmt, const void* x, int M,
+                               const void* packed_W, int64_t N, int64_t K, float* y,
+                               cudaStream_t stream);
+
 /* Capacity of qgemv_run_noalloc's scratch, in fp32 column sums: N * ceil(K / 2048) of them. */
 #define QGEMV_NOALLOC_MAX_COLUMN_SUMS 262144
 

@@ -7,6 +7,7 @@
 #include <new>
 
 #include "../../include/qgemv.h"
+#include "qgemv_batch.cuh"
 #include "qgemv_simple.cuh"
 #include "qgemv_stream.cuh"
 
@@ -37,6 +38,7 @@ struct Handle {
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
   size_t group1_smem_max[6][2][2][3] = {};  // one-format grouped kernels [format][pairs][R 2/4][D 2/3/4]
+  size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3] (Q4_K, NVFP4)
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -139,6 +141,8 @@ const void* group_kernel_pair_q6k(int R, int D);
 const void* group_kernel_pair_q80(int R, int D);
 const void* group_kernel_pair_tq10(int R, int D);
 const void* group_kernel_pair_nvfp4(int R, int D);
+const void* batch_kernel_for(int f, int D);
+size_t batch_smem_bytes(int f, int warps, int D);
 }  // namespace qg
 
 namespace {
@@ -417,6 +421,44 @@ void launch_unpack(const UnpackArgs& ua, int grid, cudaStream_t s) {
   unpack_kernel<F><<<grid, 256, 0, s>>>(ua);
 }
 
+// One single-vector GEMV on validated arguments (x 16-byte aligned; y needs no alignment).
+qgemv_status_t launch_single(const Handle& hr, int fmt, const void* x, const void* W, int64_t N, int64_t K, float* y,
+                             cudaStream_t stream) {
+  const Handle* h = &hr;
+  Plan pl;
+  qgemv_status_t st = make_plan(*h, fmt, N, K, pl);
+  if (st != QGEMV_OK) return st;
+  const uint8_t* Wb = static_cast<const uint8_t*>(W);
+  if (pl.path == 2) {
+    RowArgs ra{Wb, static_cast<const uint16_t*>(x), y, N, K, 1.f, 0.f, 0, 0, nullptr};
+    launch_rowwarp_any(fmt, pl, ra, stream);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+  }
+  StreamArgs a = pl.sa;
+  a.W = Wb;
+  a.W2 = (fmt == QGEMV_NVFP4) ? Wb + N * (K / 2) : nullptr;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = y;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid, 1, 1);
+  cfg.blockDim = dim3(pl.threads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (h->pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt, pl.R, pl.D), args) != cudaSuccess) {
+    cudaGetLastError();
+    return QGEMV_ERR_CUDA;
+  }
+  return QGEMV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -512,6 +554,21 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
             return QGEMV_ERR_CUDA;
           }
         }
+  for (int f : {static_cast<int>(F_Q4K), static_cast<int>(F_NVFP4)})
+    for (int D : {2, 3}) {
+      cudaFuncAttributes fa;
+      const void* fn = batch_kernel_for(f, D);
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+        release();
+        return QGEMV_ERR_CUDA;
+      }
+      size_t& mx = h->batch_smem_max[f][D - 2];
+      mx = h->smem_optin - std::min(h->smem_optin, fa.sharedSizeBytes);
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mx)) != cudaSuccess) {
+        release();
+        return QGEMV_ERR_CUDA;
+      }
+    }
   *out = reinterpret_cast<qgemv_handle_t>(h);
   return QGEMV_OK;
 }
@@ -596,24 +653,59 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
   if (st != QGEMV_OK) return st;
   if (!x || !y) return QGEMV_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return QGEMV_ERR_MISALIGNED;
-  Plan pl;
-  st = make_plan(*h, fmt, N, K, pl);
+  return launch_single(*h, fmt, x, W, N, K, y, stream);
+}
+
+qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, int M, const void* W, int64_t N,
+                               int64_t K, float* y, cudaStream_t stream) {
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  qgemv_status_t st = validate(h, fmt, W, N, K);
   if (st != QGEMV_OK) return st;
-  const uint8_t* Wb = static_cast<const uint8_t*>(W);
-  if (pl.path == 2) {
-    RowArgs ra{Wb, static_cast<const uint16_t*>(x), y, N, K, 1.f, 0.f, 0, 0, nullptr};
-    launch_rowwarp_any(fmt, pl, ra, stream);
-    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+  if (!x || !y || M < 1 || M > QGEMV_MAX_BATCH) return QGEMV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return QGEMV_ERR_MISALIGNED;
+  const int f = static_cast<int>(fmt);
+  int64_t rb1 = 0, rb2 = 0;
+  const int64_t Wk = (K / 256 + 7) / 8;
+  // The batch kernel: Q4_K / NVFP4 with streaming-eligible rows, its column sums in the
+  // workspace.  Otherwise each vector runs the single-vector path.
+  const bool batch = (f == F_Q4K || f == F_NVFP4) && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
+                     (Wk == 1 || static_cast<double>(M) * N * Wk <= static_cast<double>(kWsFloats));
+  if (!batch) {
+    for (int m = 0; m < M; ++m) {
+      st = launch_single(*h, f, static_cast<const uint16_t*>(x) + m * K, W, N, K, y + m * N, stream);
+      if (st != QGEMV_OK) return st;
+    }
+    return QGEMV_OK;
   }
-  StreamArgs a = pl.sa;
-  a.W = Wb;
-  a.W2 = (fmt == QGEMV_NVFP4) ? Wb + N * (K / 2) : nullptr;
+  const int warps = 8;
+  int64_t ranges = std::max<int64_t>(1, h->sms / Wk);
+  ranges = std::min<int64_t>(ranges, (N + kBatchRows - 1) / kBatchRows);
+  ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));
+  if (N / ranges >= 0x7ffffffe) return QGEMV_ERR_BAD_SHAPE;
+  int D = 3;
+  while (D > 2 && batch_smem_bytes(f, warps, D) > h->batch_smem_max[f][D - 2]) --D;
+  const size_t smem = batch_smem_bytes(f, warps, D);
+  if (smem > h->batch_smem_max[f][D - 2]) return QGEMV_ERR_BAD_SHAPE;
+  BatchArgs a{};
+  a.W = static_cast<const uint8_t*>(W);
+  a.W2 = (f == F_NVFP4) ? a.W + N * (K / 2) : nullptr;
   a.x = static_cast<const uint16_t*>(x);
   a.y = y;
+  a.N = N;
+  a.M = M;
+  a.K = static_cast<int>(K);
+  a.nsb = static_cast<int>(K / 256);
+  a.Wk = static_cast<int>(Wk);
+  a.rows_q = static_cast<int>(N / ranges);
+  a.rows_rem = static_cast<int>(N % ranges);
+  a.row_bytes = rb1;
+  a.row_bytes2 = rb2;
+  a.ws = h->ws;
+  a.cnt = h->cnt;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.grid, 1, 1);
-  cfg.blockDim = dim3(pl.threads, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
+  cfg.gridDim = dim3(static_cast<unsigned>(ranges * Wk), 1, 1);
+  cfg.blockDim = dim3(32 * warps, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (h->pdl) {
@@ -623,7 +715,7 @@ qgemv_status_t qgemv_run(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, c
     cfg.numAttrs = 1;
   }
   void* args[] = {&a};
-  if (cudaLaunchKernelExC(&cfg, stream_kernel_for(fmt, pl.R, pl.D), args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, batch_kernel_for(f, D), args) != cudaSuccess) {
     cudaGetLastError();
     return QGEMV_ERR_CUDA;
   }

@@ -1,0 +1,22 @@
+// Small-batch kernel instantiations (Q4_K and NVFP4; ring depths 2 and 3).
+#include "qgemv_batch.cuh"
+
+namespace qg {
+
+const void* batch_kernel_for(int f, int D) {
+  switch (f) {
+    case F_Q4K: return batch_kernel_table<BatchQ4K>(D);
+    case F_NVFP4: return batch_kernel_table<BatchNVFP4>(D);
+  }
+  return nullptr;
+}
+
+size_t batch_smem_bytes(int f, int warps, int D) {
+  switch (f) {
+    case F_Q4K: return batch_smem(warps, D, batch_slice<BatchQ4K>()).total;
+    case F_NVFP4: return batch_smem(warps, D, batch_slice<BatchNVFP4>()).total;
+  }
+  return 0;
+}
+
+}  // namespace qg

@@ -22,6 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_FORMAT, ERR_BAD_SHAPE, ERR_MISALIGNED, ERR_
 NOALLOC_MAX_COLUMN_SUMS = 262144  # QGEMV_NOALLOC_MAX_COLUMN_SUMS
 OUT_F32, OUT_F16, OUT_BF16 = 0, 1, 2
 MAX_GROUP = 8  # QGEMV_MAX_GROUP
+MAX_BATCH = 8  # QGEMV_MAX_BATCH
 
 
 class Problem(ctypes.Structure):
@@ -32,7 +33,7 @@ class Problem(ctypes.Structure):
 
 EXPORTS = ["qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
            "qgemv_status_string", "qgemv_packed_bytes", "qgemv_group_size", "qgemv_set_option",
-           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc", "qgemv_run_group", "qgemv_run_ex"]
+           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc", "qgemv_run_group", "qgemv_run_ex", "qgemv_run_batch"]
 
 _lib = None
 
@@ -68,9 +69,10 @@ def lib() -> ctypes.CDLL:
         L.qgemv_run_group.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.POINTER(Problem), vp]
         L.qgemv_run_ex.argtypes = [vp, ctypes.c_int, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, vp,
                                    ctypes.c_int, vp]
+        L.qgemv_run_batch.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, i64, i64, vp, vp]
         for name in ("qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
                      "qgemv_set_option", "qgemv_describe", "qgemv_run_noalloc", "qgemv_run_group",
-                     "qgemv_run_ex"):
+                     "qgemv_run_ex", "qgemv_run_batch"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -171,6 +173,14 @@ def run_ex(h: Handle, fmt: int, x, packed_W, N: int, K: int, y, alpha: float = 1
                             _stream(stream))
     if check:
         _check(st, "qgemv_run_ex")
+    return st
+
+
+def run_batch(h: Handle, fmt: int, x, M: int, packed_W, N: int, K: int, y, stream=None, check: bool = True) -> int:
+    """Y[m] = X[m] . dequant(W)^T for M (<= MAX_BATCH) row-major activation vectors x [M, K]."""
+    st = lib().qgemv_run_batch(h.ptr, fmt, _ptr(x), M, _ptr(packed_W), N, K, _ptr(y), _stream(stream))
+    if check:
+        _check(st, "qgemv_run_batch")
     return st
 
 
