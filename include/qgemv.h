@@ -250,7 +250,7 @@ qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x,
  * GEMV of the Q4_K page, "What is a GEMV", with x of shape (M, K) instead of (1, K)): every
  * packed weight is read and decoded once and serves all M vectors.  Q4_K and NVFP4 with
  * K a multiple of 256 use the tensor cores' mma.sync path (decoded weights go straight into
- * the B fragments; the M vectors fill the A operand), as long as M * N * ceil(K / 2048) fits
+ * the A fragments; the M vectors fill the B operand), as long as M * N * ceil(K / 1024) fits
  * the handle's workspace (4 Mi column sums); other formats and shapes run the single-vector
  * path once per vector. */
 #define QGEMV_MAX_BATCH 8

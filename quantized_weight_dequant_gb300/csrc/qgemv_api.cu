@@ -665,7 +665,7 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return QGEMV_ERR_MISALIGNED;
   const int f = static_cast<int>(fmt);
   int64_t rb1 = 0, rb2 = 0;
-  const int64_t Wk = (K / 256 + 7) / 8;
+  const int64_t Wk = (K / 256 + kBatchColSB - 1) / kBatchColSB;
   // The batch kernel: Q4_K / NVFP4 with streaming-eligible rows, its column sums in the
   // workspace.  Otherwise each vector runs the single-vector path.
   const bool batch = (f == F_Q4K || f == F_NVFP4) && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
@@ -677,7 +677,7 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
     }
     return QGEMV_OK;
   }
-  const int warps = 8;
+  const int warps = kBatchThreads / 32;
   int64_t ranges = std::max<int64_t>(1, h->sms / Wk);
   ranges = std::min<int64_t>(ranges, (N + kBatchRows - 1) / kBatchRows);
   ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));

@@ -4,24 +4,25 @@
 // At M = 1 the product is a matrix-vector product and the streaming kernel's integer dot
 // products fit it best ("fp4_gemv" page: no MMA at M = 1); from a few vectors on, the same
 // decoded weight meets several activations, which is what the tensor cores' mma.sync
-// contraction does without any shared-memory round trip: the weights are decoded in
-// registers straight into the B fragments of m16n8k16 (8 weight rows as its N) and the
-// activation vectors are its M (16 slots, M of them used).
+// contraction does without any shared-memory round trip for the weights: they are decoded
+// in registers straight into the A fragments of m16n8k16 (16 weight rows as its M), and the
+// activation vectors are its N (8 slots, M of them used).
 //
-//  * Work split as in the streaming kernel's split mode: a CTA takes one 2048-wide
-//    K-column of a row range; warp p takes row group p of the range, 8 rows per stage,
-//    through a private ring of D stages filled with 16-byte cp.async copies.
-//  * Activations: the CTA stages its K-column of all M vectors once, already in the
-//    A-fragment order (lane (g, t4) reads the pair of fp16 values for vector g at its k
-//    slots with one 8-byte shared load per k-step).  Unused vector slots hold zeros.
-//  * Lane (g, t4) decodes row g of a stage, 64 elements of each superblock (chunk t4), and
-//    gets back the sums of rows 2 t4 and 2 t4 + 1 for vector g from the accumulator.
-//  * Q4_K: B = q * s_g, an exact integer <= 945 in fp16 (the 6-bit group scale folded in):
+//  * Work split: a CTA takes one 1024-wide K-column (4 superblocks) of a row range; warp p
+//    takes row group p of the range, 16 rows per stage, through a private ring of D stages
+//    filled with 16-byte cp.async copies (row slots padded so the 16 rows of a stage start
+//    in different shared-memory banks).
+//  * Activations: the CTA stages its K-column of all M vectors once, already in B-fragment
+//    order (lane (g, t4) reads the pair of fp16 values for vector g at its k slots with one
+//    8-byte shared load per k-step).  Unused vector slots hold zeros.
+//  * Lane (g, t4) decodes rows g and g + 8 of a stage, 64 elements of each superblock
+//    (chunk t4), and receives the sums of those rows for vectors 2 t4 and 2 t4 + 1.
+//  * Q4_K: A = q * s_g, an exact integer <= 945 in fp16 (the 6-bit group scale folded in):
 //    one LOP3 puts two nibbles into fp16 (1024 + q) / (1024 + 16 q), one fused multiply-add
 //    scales and removes the offset.  The group minimum term sum_g m_g X_g goes through an
-//    m16n8k8 product (A = the group sums of x split into two fp16 parts, B = m_g), and the
+//    m16n8k8 product (A = m_g, B = the group sums of x split into two fp16 parts), and the
 //    superblock scales d, dmin are applied to both sums in fp32 once per superblock.
-//  * NVFP4: B = e2m1 * |e4m3 block scale|, exact in fp16; x (bf16) is staged as fp16 times
+//  * NVFP4: A = e2m1 * |e4m3 block scale|, exact in fp16; x (bf16) is staged as fp16 times
 //    2^sigma per vector and K-column (sigma from the column's largest |x|), and the sums are
 //    scaled back when written.
 //  * Results: with one K-column they are written to Y; otherwise every CTA writes its
@@ -38,8 +39,10 @@
 
 namespace qg {
 
-constexpr int kBatchMax = 8;  // activation vectors (the MMA's M slots used)
-constexpr int kBatchRows = 8;  // weight rows per stage (the MMA's N)
+constexpr int kBatchMax = 8;        // activation vectors (the MMA's N)
+constexpr int kBatchRows = 16;      // weight rows per stage (the MMA's M)
+constexpr int kBatchColSB = 4;      // superblocks per K-column
+constexpr int kBatchThreads = 256;  // 8 warps per CTA
 
 struct BatchArgs {
   const uint8_t* W;   // stream 1: packed blocks / NVFP4 nibbles
@@ -50,41 +53,44 @@ struct BatchArgs {
   int M;
   int K;
   int nsb;            // superblocks per row
-  int Wk;             // K-columns = ceil(nsb / 8)
+  int Wk;             // K-columns = ceil(nsb / 4)
   int rows_q, rows_rem;  // range b has rows_q (+1 if b < rows_rem) rows
   int64_t row_bytes, row_bytes2;
   float* ws;          // Wk > 1: column sums [Wk][M][N]
   int* cnt;           // per-range arrival counts, zero between launches
 };
 
-// Shared memory: [rings: warps * D * 8 * slice][x fragments: 8 sb * 16 steps * 32 lanes * 8 B]
-// [group sums (Q4_K): 8 sb * 32 lanes * 8 B][per-vector scales 2^-sigma: 8 floats][flag].
+// Shared memory: [rings: warps * D * 16 * slot][x fragments: 4 sb * 16 steps * 32 lanes * 8 B]
+// [group sums (Q4_K): 4 sb * 32 lanes * 8 B][per-vector sigma: 8 ints].
 struct BatchSmem {
   size_t xa, xs, sc, total;
 };
 __host__ __device__ inline BatchSmem batch_smem(int warps, int D, int slice) {
   BatchSmem m;
   m.xa = static_cast<size_t>(warps) * D * kBatchRows * slice;
-  m.xs = m.xa + 8 * 16 * 32 * 8;
-  m.sc = m.xs + 8 * 32 * 8;
+  m.xs = m.xa + kBatchColSB * 16 * 32 * 8;
+  m.sc = m.xs + kBatchColSB * 32 * 8;
   m.total = m.sc + kBatchMax * 4 + 16;
   return m;
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  const uint32_t z = 0u;  // vector slots 8..15 are unused
+// D += A B: A fragment {a0: row g, k 2t4..2t4+1; a1: row g+8; a2: row g, k 2t4+8..; a3: row
+// g+8, k 2t4+8..}, B fragment {b0: k 2t4..2t4+1, column g; b1: k 2t4+8..}, D {row g, columns
+// 2t4, 2t4+1; row g+8, columns 2t4, 2t4+1} (fp16 pairs, fp32 accumulators).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t b0) {
-  const uint32_t z = 0u;
+// The k = 8 form: A {a0: row g, k 2t4..2t4+1; a1: row g+8}, B {b0: k 2t4..2t4+1, column g}.
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
   asm volatile(
       "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(z), "r"(b0));
+      : "r"(a0), "r"(a1), "r"(b0));
 }
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -105,6 +111,15 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
+}
+
+// (a & mask) | c in one LOP3 (c a register: the compiler would otherwise spend a second
+// logic op on a second immediate).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
 }
 
 // Two small non-negative integers (< 1024) as the fp16 pair (lo, hi), exactly.
@@ -129,57 +144,66 @@ struct BatchQ4K {
     v.y = __byte_perm(raw.x, raw.y, 0x7632);  // (x1, x3)
   }
 
-  // Lane (g, t4) of a warp: the superblock at shared address `blk` of row g; `hd0`, `hd1`
-  // the first words (d, dmin) of rows 2 t4 and 2 t4 + 1; xa / xs its fragment addresses.
-  __device__ __forceinline__ static void superblock(uint32_t blk, uint32_t hd0, uint32_t hd1, int t4,
-                                                    uint32_t xa, uint32_t xs, float& acc0, float& acc1) {
-    const uint4 hdr = lds_v4(blk);
-    const uint4 q0 = lds_v4(blk + 16 + 32 * t4), q1 = lds_v4(blk + 32 + 32 * t4);
-    // 6-bit scales and mins of groups 2 t4 and 2 t4 + 1 ("Kernel code" mask arithmetic)
-    uint32_t sl, sh, ml, mh;
-    {
-      const int jl = 2 * t4, jh = 2 * t4 + 1;
-      const int ql = jl & 3, qh = jh & 3;
-      const uint32_t S0 = hdr.y, S1 = hdr.z, S2 = hdr.w;
-      auto byte_of = [](uint32_t w, int q) { return (w >> (8 * q)) & 0xFFu; };
-      if (t4 < 2) {
-        sl = byte_of(S0, ql) & 63u;
-        sh = byte_of(S0, qh) & 63u;
-        ml = byte_of(S1, ql) & 63u;
-        mh = byte_of(S1, qh) & 63u;
-      } else {
-        sl = (byte_of(S2, ql) & 15u) | ((byte_of(S0, ql) >> 6) << 4);
-        sh = (byte_of(S2, qh) & 15u) | ((byte_of(S0, qh) >> 6) << 4);
-        ml = (byte_of(S2, ql) >> 4) | ((byte_of(S1, ql) >> 6) << 4);
-        mh = (byte_of(S2, qh) >> 4) | ((byte_of(S1, qh) >> 6) << 4);
-      }
-    }
-    const uint32_t S = int2_to_h2(sl, sh);                       // (s_lo, s_hi)
-    const uint32_t SL = __byte_perm(S, S, 0x1010);               // (s_lo, s_lo)
-    const uint32_t SH = hmul2_u(__byte_perm(S, S, 0x3232), 0x2C002C00u);  // s_hi / 16
-    const uint32_t CL = hmul2_u(SL, 0xE400E400u);                // -1024 s_lo
-    const uint32_t CH = hmul2_u(SH, 0xE400E400u);                // -64 s_hi
-    const uint32_t Bm = int2_to_h2(ml, mh);                      // (m_lo, m_hi)
-    float dq[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  // Scales and mins of groups 2 t4 and 2 t4 + 1 from a block header (12 packed bytes in
+  // hdr.y..w; "Kernel code" mask arithmetic) as fp16 pairs (lo group, hi group).  Groups 0..3
+  // take the low 6 bits of bytes 0..3 / 4..7; groups 4..7 a nibble of bytes 8..11 below the
+  // top two bits of bytes 0..3 / 4..7.  Selects, so the warp does not diverge.
+  __device__ __forceinline__ static void group_scales(const uint4& hdr, int t4, uint32_t& S, uint32_t& Mn) {
+    const uint32_t sh16 = 16u * (t4 & 1);  // byte q = 2 (t4 & 1) in bits 0..7, byte q + 1 in 8..15
+    const uint32_t B0 = hdr.y >> sh16, B1 = hdr.z >> sh16, B2 = hdr.w >> sh16;
+    const uint32_t c0 = B0 & 0xFFu, c1 = (B0 >> 8) & 0xFFu;  // S0[q], S0[q + 1]
+    const uint32_t e0 = B1 & 0xFFu, e1 = (B1 >> 8) & 0xFFu;  // S1[q], S1[q + 1]
+    const uint32_t f0 = B2 & 0xFFu, f1 = (B2 >> 8) & 0xFFu;  // S2[q], S2[q + 1]
+    const bool split = t4 >= 2;
+    const uint32_t sl = split ? ((f0 & 15u) | ((c0 >> 6) << 4)) : (c0 & 63u);
+    const uint32_t sh = split ? ((f1 & 15u) | ((c1 >> 6) << 4)) : (c1 & 63u);
+    const uint32_t ml = split ? ((f0 >> 4) | ((e0 >> 6) << 4)) : (e0 & 63u);
+    const uint32_t mh = split ? ((f1 >> 4) | ((e1 >> 6) << 4)) : (e1 & 63u);
+    S = int2_to_h2(sl, sh);
+    Mn = int2_to_h2(ml, mh);
+  }
+
+  // Lane (g, t4): the superblock at shared addresses `bg` (row g) and `b8` (row g + 8); xa / xs
+  // its fragment addresses.  Adds the superblock's contribution to the lane's four sums.
+  __device__ __forceinline__ static void superblock(uint32_t bg, uint32_t b8, int t4, uint32_t xa, uint32_t xs,
+                                                    uint32_t magic, float (&y)[4]) {
+    const uint4 hg = lds_v4(bg), h8 = lds_v4(b8);
+    const uint4 g0 = lds_v4(bg + 16 + 32 * t4), g1 = lds_v4(bg + 32 + 32 * t4);
+    const uint4 e0 = lds_v4(b8 + 16 + 32 * t4), e1 = lds_v4(b8 + 32 + 32 * t4);
+    uint32_t Sg, Mg, S8, M8;
+    group_scales(hg, t4, Sg, Mg);
+    group_scales(h8, t4, S8, M8);
+    // low-nibble pairs: (1024 + q) s - 1024 s; high-nibble pairs: (1024 + 16 q) s/16 - 64 s
+    const uint32_t SLg = __byte_perm(Sg, Sg, 0x1010), SL8 = __byte_perm(S8, S8, 0x1010);
+    const uint32_t SHg = hmul2_u(__byte_perm(Sg, Sg, 0x3232), 0x2C002C00u);
+    const uint32_t SH8 = hmul2_u(__byte_perm(S8, S8, 0x3232), 0x2C002C00u);
+    const uint32_t CLg = hmul2_u(SLg, 0xE400E400u), CL8 = hmul2_u(SL8, 0xE400E400u);
+    const uint32_t CHg = hmul2_u(SHg, 0xE400E400u), CH8 = hmul2_u(SH8, 0xE400E400u);
+    const uint32_t wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t w8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    float dq[2][4] = {};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t w0 = w[i], w8 = w[i] >> 8;
-      const uint32_t l0 = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, SL, CL);
-      const uint32_t l1 = hfma2_u((w8 & 0x000F000Fu) | 0x64006400u, SL, CL);
-      const uint32_t h0 = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, SH, CH);
-      const uint32_t h1 = hfma2_u((w8 & 0x00F000F0u) | 0x64006400u, SH, CH);
+      const uint32_t a = wg[i], a8 = wg[i] >> 8, b = w8[i], b8s = w8[i] >> 8;
       const uint2 xl = lds_v2(xa + (2 * i) * 256), xh = lds_v2(xa + (2 * i + 1) * 256);
-      mma16816(dq, xl.x, xl.y, l0, l1);
-      mma16816(dq, xh.x, xh.y, h0, h1);
+      mma16816(dq[0], hfma2_u(and_or<0x000F000Fu>(a, magic), SLg, CLg),
+               hfma2_u(and_or<0x000F000Fu>(b, magic), SL8, CL8),
+               hfma2_u(and_or<0x000F000Fu>(a8, magic), SLg, CLg),
+               hfma2_u(and_or<0x000F000Fu>(b8s, magic), SL8, CL8), xl.x, xl.y);
+      mma16816(dq[1], hfma2_u(and_or<0x00F000F0u>(a, magic), SHg, CHg),
+               hfma2_u(and_or<0x00F000F0u>(b, magic), SH8, CH8),
+               hfma2_u(and_or<0x00F000F0u>(a8, magic), SHg, CHg),
+               hfma2_u(and_or<0x00F000F0u>(b8s, magic), SH8, CH8), xh.x, xh.y);
     }
-    float dm[4] = {0.f, 0.f, 0.f, 0.f};
+    float dm[4] = {};
     const uint2 X = lds_v2(xs);  // group sums / 64: (hi parts), (lo parts)
-    mma1688(dm, X.x, Bm);
-    mma1688(dm, X.y, Bm);
-    const float d0 = h2f(hd0), m0 = h2f(hd0 >> 16) * 64.f, d1 = h2f(hd1), m1 = h2f(hd1 >> 16) * 64.f;
-    acc0 += fmaf(d0, dq[0], -m0 * dm[0]);
-    acc1 += fmaf(d1, dq[1], -m1 * dm[1]);
+    mma1688(dm, Mg, M8, X.x);
+    mma1688(dm, Mg, M8, X.y);
+    const float dg = h2f(hg.x), mg = h2f(hg.x >> 16) * 64.f, d8 = h2f(h8.x), m8 = h2f(h8.x >> 16) * 64.f;
+    y[0] += fmaf(dg, dq[0][0] + dq[1][0], -mg * dm[0]);
+    y[1] += fmaf(dg, dq[0][1] + dq[1][1], -mg * dm[1]);
+    y[2] += fmaf(d8, dq[0][2] + dq[1][2], -m8 * dm[2]);
+    y[3] += fmaf(d8, dq[0][3] + dq[1][3], -m8 * dm[3]);
   }
 };
 
@@ -196,38 +220,46 @@ struct BatchNVFP4 {
     v = raw;
   }
 
-  __device__ __forceinline__ static void superblock(uint32_t nib, uint32_t sc, int t4, uint32_t xa, float (&dq)[4]) {
-    const uint4 q0 = lds_v4(nib + 32 * t4), q1 = lds_v4(nib + 32 * t4 + 16);
-    const uint32_t s4 = lds_u32(sc + 4 * t4) & 0x7F7F7F7Fu;  // |scale| of blocks 4 t4 .. 4 t4 + 3
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  // Rows g (nibbles at ng, scales at sg) and g + 8 (n8, s8) of a superblock.
+  __device__ __forceinline__ static void superblock(uint32_t ng, uint32_t n8, uint32_t sg, uint32_t s8, int t4,
+                                                    uint32_t xa, float (&dq)[2][4]) {
+    const uint4 g0 = lds_v4(ng + 32 * t4), g1 = lds_v4(ng + 32 * t4 + 16);
+    const uint4 e0 = lds_v4(n8 + 32 * t4), e1 = lds_v4(n8 + 32 * t4 + 16);
+    const uint32_t sG = lds_u32(sg + 4 * t4) & 0x7F7F7F7Fu;  // |scale| of blocks 4 t4 .. 4 t4 + 3
+    const uint32_t s8v = lds_u32(s8 + 4 * t4) & 0x7F7F7F7Fu;
+    const uint32_t wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t w8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t sh = DecNVFP4::e4m3x2((s4 >> (8 * b)) & 0xFFu);
-      const uint32_t sv = __byte_perm(sh, sh, 0x1010);
+      const uint32_t tg = DecNVFP4::e4m3x2((sG >> (8 * b)) & 0xFFu), t8 = DecNVFP4::e4m3x2((s8v >> (8 * b)) & 0xFFu);
+      const uint32_t vg = __byte_perm(tg, tg, 0x1010), v8 = __byte_perm(t8, t8, 0x1010);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int i = 2 * b + u;
-        uint32_t h[4];
-        DecNVFP4::e2m1x8(w[i], h);
+        uint32_t hg[4], h8[4];
+        DecNVFP4::e2m1x8(wg[i], hg);
+        DecNVFP4::e2m1x8(w8[i], h8);
         const uint2 xl = lds_v2(xa + (2 * i) * 256), xh = lds_v2(xa + (2 * i + 1) * 256);
-        mma16816(dq, xl.x, xl.y, hmul2_u(h[0], sv), hmul2_u(h[1], sv));
-        mma16816(dq, xh.x, xh.y, hmul2_u(h[2], sv), hmul2_u(h[3], sv));
+        mma16816(dq[0], hmul2_u(hg[0], vg), hmul2_u(h8[0], v8), hmul2_u(hg[1], vg), hmul2_u(h8[1], v8), xl.x, xl.y);
+        mma16816(dq[1], hmul2_u(hg[2], vg), hmul2_u(h8[2], v8), hmul2_u(hg[3], vg), hmul2_u(h8[3], v8), xh.x, xh.y);
       }
     }
   }
 };
 
+// Bytes of one row slot in a ring stage: the row's 4-superblock slice plus 16 bytes, so that
+// the 16 rows of a stage start in different shared-memory banks.
 template <class Fmt>
 __host__ __device__ constexpr int batch_slice() {
-  return 8 * Fmt::kSB + 8 * Fmt::kSB2;
+  return kBatchColSB * (Fmt::kSB + Fmt::kSB2) + 16;
 }
 
 template <class Fmt, int D>
-__global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ BatchArgs a) {
+__global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_constant__ BatchArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = Fmt::kSB, SB2 = Fmt::kSB2, SLICE = batch_slice<Fmt>();
   constexpr int STAGE = kBatchRows * SLICE;
-  constexpr int J1 = (8 * SB / 16 + 31) / 32, J2 = (8 * SB2 / 16 + 31) / 32;
+  constexpr int J1 = (kBatchColSB * SB / 16 + 31) / 32, J2 = (kBatchColSB * SB2 / 16 + 31) / 32;
   constexpr bool kIsNVFP4 = SB2 > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t4 = lane & 3;
@@ -238,7 +270,7 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
   const int pq = ncta / nwarps, prem = ncta % nwarps;
   const int64_t p_lo = r_lo + warp * pq + min(warp, prem);
   const int nrows = pq + (warp < prem ? 1 : 0);
-  const int ncols = min(8, a.nsb - 8 * wk);  // superblocks in this K-column
+  const int ncols = min(kBatchColSB, a.nsb - kBatchColSB * wk);  // superblocks in this K-column
   const BatchSmem L = batch_smem(nwarps, D, SLICE);
   const uint32_t ring_sa = smem_u32(smem) + static_cast<uint32_t>(warp) * D * STAGE, ring_end = ring_sa + D * STAGE;
   const uint32_t xa_sa = smem_u32(smem + L.xa), xs_sa = smem_u32(smem + L.xs);
@@ -254,8 +286,9 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
 #pragma unroll
   for (int j = 0; j < J2; ++j) ok2[j] = lane + 32 * j < n2;
   const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
-  const uint8_t* gi1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * 8 * SB + 16 * lane;
-  const uint8_t* gi2 = kIsNVFP4 ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * 8 * SB2 + 16 * lane : a.W;
+  const uint8_t* gi1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * kBatchColSB * SB + 16 * lane;
+  const uint8_t* gi2 =
+      kIsNVFP4 ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * kBatchColSB * SB2 + 16 * lane : a.W;
   const int nst = (nrows + kBatchRows - 1) / kBatchRows, nfull = nrows / kBatchRows;
   const int tail = nrows - nfull * kBatchRows;
   auto copy_row = [&](uint32_t d, const uint8_t* s1, const uint8_t* s2) {
@@ -271,7 +304,7 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
     }
     if constexpr (kIsNVFP4) {
 #pragma unroll
-      for (int j = 0; j < J2; ++j) cp_async16_if<8 * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
+      for (int j = 0; j < J2; ++j) cp_async16_if<kBatchColSB * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
     }
   };
   auto issue = [&](int st, uint32_t slot_sa) {
@@ -286,66 +319,77 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
     }
     cp_async_commit();
   };
-  static_assert(J1 <= 5, "row slice of at most 160 16-byte chunks");
+  static_assert(J1 <= 5 && J2 <= 1, "row slice of at most 160 16-byte chunks");
 
   // Weight stages first (they do not depend on the previous kernel), then x.
 #pragma unroll 1
   for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
   pdl_wait();
 
-  // ---- x staging: the CTA's K-column of every vector, in fragment order.
-  const int kc0 = 2048 * wk;
+  // ---- x staging: the CTA's K-column of every vector, in fragment order.  Thread t handles
+  // the 4-value chunks t + 256 k of the 8 x 256 chunks: all its loads are issued first, so
+  // their latencies overlap.
+  const int kc0 = 256 * kBatchColSB * wk;
+  constexpr int kChunks = 64 * kBatchColSB;  // 4-value chunks per vector in the K-column
+  constexpr int kItems = kBatchMax * kChunks / kBatchThreads;
+  uint2 raw[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int idx = threadIdx.x + kBatchThreads * k, v = idx / kChunks, c = idx % kChunks;
+    raw[k] = make_uint2(0u, 0u);
+    if (v < a.M && (c >> 6) < ncols)
+      raw[k] = __ldcg(reinterpret_cast<const uint2*>(a.x + static_cast<int64_t>(v) * a.K + kc0) + c);
+  }
   if constexpr (kIsNVFP4) {
     // per vector: sigma with max |x| * 2^sigma in [2^14, 2^15) over this K-column
     int* const vmax = reinterpret_cast<int*>(vscale);
     if (threadIdx.x < kBatchMax) vmax[threadIdx.x] = 0;
     __syncthreads();
-    for (int idx = threadIdx.x; idx < a.M * 512; idx += blockDim.x) {
-      const int v = idx >> 9, c = idx & 511;
-      if (4 * c < 256 * ncols) {
-        const uint2 r = __ldcg(reinterpret_cast<const uint2*>(a.x + static_cast<int64_t>(v) * a.K + kc0) + c);
-        const uint32_t m = max(max(r.x & 0x7FFFu, (r.x >> 16) & 0x7FFFu), max(r.y & 0x7FFFu, (r.y >> 16) & 0x7FFFu));
-        if (m) atomicMax(vmax + v, static_cast<int>(m));
-      }
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int v = (threadIdx.x + kBatchThreads * k) / kChunks;  // uniform over the warp
+      uint32_t m = max(max(raw[k].x & 0x7FFFu, (raw[k].x >> 16) & 0x7FFFu),
+                       max(raw[k].y & 0x7FFFu, (raw[k].y >> 16) & 0x7FFFu));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0 && m) atomicMax(vmax + v, static_cast<int>(m));
     }
     __syncthreads();
     if (threadIdx.x < kBatchMax) {
       const int m = vmax[threadIdx.x];
       const int e8 = (m >> 7) & 0xFF;  // bf16 biased exponent of the largest |x|
-      reinterpret_cast<int*>(vscale)[threadIdx.x] = m ? max(-100, min(100, 141 - e8)) : 0;  // sigma
+      vmax[threadIdx.x] = m ? max(-100, min(100, 141 - e8)) : 0;  // sigma
     }
     __syncthreads();
   }
-  for (int idx = threadIdx.x; idx < kBatchMax * 512; idx += blockDim.x) {
-    const int v = idx >> 9, c = idx & 511;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int idx = threadIdx.x + kBatchThreads * k, v = idx / kChunks, c = idx % kChunks;
     const int sb = c >> 6, e = 4 * (c & 63);
-    uint2 raw = make_uint2(0u, 0u);
-    if (v < a.M && sb < ncols) {
-      raw = __ldcg(reinterpret_cast<const uint2*>(a.x + static_cast<int64_t>(v) * a.K + kc0) + c);
-      if constexpr (kIsNVFP4) {
-        const float f = p2(reinterpret_cast<const int*>(vscale)[v]);
-        const __half2 h0 = __floats2half2_rn(bf2f(raw.x) * f, bf2f(raw.x >> 16) * f);
-        const __half2 h1 = __floats2half2_rn(bf2f(raw.y) * f, bf2f(raw.y >> 16) * f);
-        raw = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-      }
+    uint2 r = raw[k];
+    if constexpr (kIsNVFP4) {
+      const float f = p2(reinterpret_cast<const int*>(vscale)[v]);
+      const __half2 h0 = __floats2half2_rn(bf2f(r.x) * f, bf2f(r.x >> 16) * f);
+      const __half2 h1 = __floats2half2_rn(bf2f(r.y) * f, bf2f(r.y >> 16) * f);
+      r = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
     }
     int step, tq;
     uint2 val;
-    Fmt::chunk_slot(e, step, tq, val, raw);
+    Fmt::chunk_slot(e, step, tq, val, r);
     const int ln = 4 * v + tq;
     *reinterpret_cast<uint2*>(smem + L.xa + ((sb * 16 + step) * 32 + ln) * 8) = val;
     if constexpr (!kIsNVFP4) {
       // group sums of x (for the minimum term): 8 chunks of 4 make a group of 32
-      float s = __half2float(__ushort_as_half(static_cast<unsigned short>(raw.x & 0xFFFFu))) +
-                __half2float(__ushort_as_half(static_cast<unsigned short>(raw.x >> 16))) +
-                __half2float(__ushort_as_half(static_cast<unsigned short>(raw.y & 0xFFFFu))) +
-                __half2float(__ushort_as_half(static_cast<unsigned short>(raw.y >> 16)));
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      float gs = __half2float(__ushort_as_half(static_cast<unsigned short>(r.x & 0xFFFFu))) +
+                 __half2float(__ushort_as_half(static_cast<unsigned short>(r.x >> 16))) +
+                 __half2float(__ushort_as_half(static_cast<unsigned short>(r.y & 0xFFFFu))) +
+                 __half2float(__ushort_as_half(static_cast<unsigned short>(r.y >> 16)));
+      gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 4);
       if ((c & 7) == 0) {
         const int grp = e >> 5;  // group of the superblock: the m16n8k8 k index
-        const float sc = s * (1.0f / 64.0f);  // keeps the fp16 parts finite for any fp16 x
+        const float sc = gs * (1.0f / 64.0f);  // keeps the fp16 parts finite for any fp16 x
         const __half hi = __float2half_rn(sc);
         const __half lo = __float2half_rn(sc - __half2float(hi));
         uint16_t* dst = reinterpret_cast<uint16_t*>(smem + L.xs + (sb * 32 + 4 * v + (grp >> 1)) * 8);
@@ -355,38 +399,51 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
     }
   }
   __syncthreads();
-  float oscale = 1.f;  // output scale of this lane's vector g
-  if constexpr (kIsNVFP4) oscale = p2(-reinterpret_cast<const int*>(vscale)[g]);
+  // output scales of this lane's vectors 2 t4 and 2 t4 + 1 (NVFP4: 2^-sigma)
+  float osc0 = 1.f, osc1 = 1.f;
+  if constexpr (kIsNVFP4) {
+    osc0 = p2(-reinterpret_cast<const int*>(vscale)[2 * t4]);
+    osc1 = p2(-reinterpret_cast<const int*>(vscale)[2 * t4 + 1]);
+  }
 
-  // ---- main loop: 8 rows per stage, every superblock of the K-column.
+  // ---- main loop: 16 rows per stage, every superblock of the K-column.
   float* const out = a.Wk == 1 ? a.y + p_lo : a.ws + (static_cast<int64_t>(wk) * a.M) * a.N + p_lo;
-  const bool writer = g < a.M;
+  const int v0 = 2 * t4, v1 = 2 * t4 + 1;  // this lane's vectors
+  uint32_t magic;  // fp16 (1024, 1024): the exponent under which two nibbles become fp16
+  asm("mov.b32 %0, 0x64006400;" : "=r"(magic));
   uint32_t cs = ring_sa, is = ring_sa + (D - 1) * STAGE;
   const uint32_t xa_lane = xa_sa + lane * 8, xs_lane = xs_sa + lane * 8;
   for (int st = 0; st < nst; ++st) {
     issue(st + D - 1, is);
     cp_async_wait<D - 1>();
     __syncwarp();
-    float acc0 = 0.f, acc1 = 0.f;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, v0), (row g, v1), (row g + 8, v0), (row g + 8, v1)
+    const uint32_t rg = cs + g * SLICE, r8 = cs + (g + 8) * SLICE;
     if constexpr (!kIsNVFP4) {
-      for (int c = 0; c < ncols; ++c) {
-        const uint32_t hd0 = lds_u32(cs + (2 * t4) * SLICE + SB * c);
-        const uint32_t hd1 = lds_u32(cs + (2 * t4 + 1) * SLICE + SB * c);
-        Fmt::superblock(cs + g * SLICE + SB * c, hd0, hd1, t4, xa_lane + c * 16 * 256, xs_lane + c * 256, acc0, acc1);
-      }
+#pragma unroll
+      for (int c = 0; c < kBatchColSB; ++c)
+        if (c < ncols)
+          BatchQ4K::superblock(rg + SB * c, r8 + SB * c, t4, xa_lane + c * 16 * 256, xs_lane + c * 256, magic, y);
     } else {
-      float dq[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < ncols; ++c)
-        BatchNVFP4::superblock(cs + g * SLICE + SB * c, cs + g * SLICE + 8 * SB + SB2 * c, t4, xa_lane + c * 16 * 256, dq);
-      acc0 = dq[0] * oscale;
-      acc1 = dq[1] * oscale;
+      float dq[2][4] = {};
+#pragma unroll
+      for (int c = 0; c < kBatchColSB; ++c)
+        if (c < ncols)
+          BatchNVFP4::superblock(rg + SB * c, r8 + SB * c, rg + kBatchColSB * SB + SB2 * c,
+                               r8 + kBatchColSB * SB + SB2 * c, t4, xa_lane + c * 16 * 256, dq);
+      y[0] = (dq[0][0] + dq[1][0]) * osc0;
+      y[1] = (dq[0][1] + dq[1][1]) * osc1;
+      y[2] = (dq[0][2] + dq[1][2]) * osc0;
+      y[3] = (dq[0][3] + dq[1][3]) * osc1;
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
     is = cs;
     cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;
-    const int r0 = st * kBatchRows + 2 * t4;
-    if (writer && r0 < nrows) out[static_cast<int64_t>(g) * a.N + r0] = acc0;
-    if (writer && r0 + 1 < nrows) out[static_cast<int64_t>(g) * a.N + r0 + 1] = acc1;
+    const int r0 = st * kBatchRows + g, r1 = r0 + 8;
+    if (v0 < a.M && r0 < nrows) out[static_cast<int64_t>(v0) * a.N + r0] = y[0];
+    if (v1 < a.M && r0 < nrows) out[static_cast<int64_t>(v1) * a.N + r0] = y[1];
+    if (v0 < a.M && r1 < nrows) out[static_cast<int64_t>(v0) * a.N + r1] = y[2];
+    if (v1 < a.M && r1 < nrows) out[static_cast<int64_t>(v1) * a.N + r1] = y[3];
   }
   cp_async_wait<0>();
 
@@ -400,11 +457,26 @@ __global__ void __launch_bounds__(256, 1) batch_kernel(const __grid_constant__ B
     }
     __syncthreads();
     if (last) {
-      for (int i = threadIdx.x; i < ncta * a.M; i += blockDim.x) {
-        const int v = i / ncta, r = i - v * ncta;
-        float s = 0.f;
-        for (int w = 0; w < a.Wk; ++w) s += __ldcg(a.ws + (static_cast<int64_t>(w) * a.M + v) * a.N + r_lo + r);
-        a.y[static_cast<int64_t>(v) * a.N + r_lo + r] = s;
+      // Every (vector, row) of the range: the Wk column sums added in column order.  Four
+      // outputs per thread and pass, so their loads are in flight together.
+      const int total = ncta * a.M;
+      for (int i0 = threadIdx.x; i0 < total; i0 += 4 * kBatchThreads) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = min(i0 + u * kBatchThreads, total - 1);
+          const int v = i / ncta;
+          o[u] = static_cast<int64_t>(v) * a.N + r_lo + (i - v * ncta);
+        }
+        for (int w = 0; w < a.Wk; ++w) {
+          const float* col = a.ws + static_cast<int64_t>(w) * a.M * a.N;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) s[u] += __ldcg(col + o[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i0 + u * kBatchThreads < total) a.y[o[u]] = s[u];
       }
       if (threadIdx.x == 0) a.cnt[b] = 0;
     }
