@@ -8,10 +8,10 @@
 // in registers straight into the A fragments of m16n8k16 (16 weight rows as its M), and the
 // activation vectors are its N (8 slots, M of them used).
 //
-//  * Work split: a CTA takes one 1024-wide K-column (4 superblocks) of a row range; warp p
-//    takes row group p of the range, 16 rows per stage, through a private ring of D stages
-//    filled with 16-byte cp.async copies (row slots padded so the 16 rows of a stage start
-//    in different shared-memory banks).
+//  * Work split: a CTA (16 warps) takes one 1024-wide K-column (4 superblocks) of a row
+//    range; warp p takes row group p of the range in tiles of 16 rows, each tile in stages
+//    of 2 superblocks, through a private ring of D stages filled with 16-byte cp.async
+//    copies (row slots padded so the 16 rows of a stage start in different banks).
 //  * Activations: the CTA stages its K-column of all M vectors once, already in B-fragment
 //    order (lane (g, t4) reads the pair of fp16 values for vector g at its k slots with one
 //    8-byte shared load per k-step).  Unused vector slots hold zeros.
@@ -42,7 +42,8 @@ namespace qg {
 constexpr int kBatchMax = 8;        // activation vectors (the MMA's N)
 constexpr int kBatchRows = 16;      // weight rows per stage (the MMA's M)
 constexpr int kBatchColSB = 4;      // superblocks per K-column
-constexpr int kBatchThreads = 256;  // 8 warps per CTA
+constexpr int kBatchStageSB = 2;    // superblocks per stage (a tile of 16 rows takes 1 or 2)
+constexpr int kBatchThreads = 512;  // 16 warps per CTA
 
 struct BatchArgs {
   const uint8_t* W;   // stream 1: packed blocks / NVFP4 nibbles
@@ -247,11 +248,11 @@ struct BatchNVFP4 {
   }
 };
 
-// Bytes of one row slot in a ring stage: the row's 4-superblock slice plus 16 bytes, so that
-// the 16 rows of a stage start in different shared-memory banks.
+// Bytes of one row slot in a ring stage: the row's 2 superblocks (stream 1, then stream 2)
+// plus 16 bytes, so that the 16 rows of a stage start in different shared-memory banks.
 template <class Fmt>
 __host__ __device__ constexpr int batch_slice() {
-  return kBatchColSB * (Fmt::kSB + Fmt::kSB2) + 16;
+  return kBatchStageSB * (Fmt::kSB + Fmt::kSB2) + 16;
 }
 
 template <class Fmt, int D>
@@ -259,7 +260,6 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = Fmt::kSB, SB2 = Fmt::kSB2, SLICE = batch_slice<Fmt>();
   constexpr int STAGE = kBatchRows * SLICE;
-  constexpr int J1 = (kBatchColSB * SB / 16 + 31) / 32, J2 = (kBatchColSB * SB2 / 16 + 31) / 32;
   constexpr bool kIsNVFP4 = SB2 > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t4 = lane & 3;
@@ -278,48 +278,45 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
 
   pdl_launch_dependents();
 
-  // Copies: lane chunk j of a row slice is bytes [16 lane + 512 j, +16).
-  const int n1 = ncols * SB / 16, n2 = ncols * SB2 / 16;
-  uint32_t ok1[J1], ok2[J2 > 0 ? J2 : 1];
-#pragma unroll
-  for (int j = 0; j < J1; ++j) ok1[j] = lane + 32 * j < n1;
-#pragma unroll
-  for (int j = 0; j < J2; ++j) ok2[j] = lane + 32 * j < n2;
+  // Copies.  A stage is 16 rows x CPR 16-byte chunks (2 superblocks of stream 1, then of
+  // stream 2); lane l copies chunks l + 32 j, whose row, source offset (from the stage's row
+  // block) and slot offset are fixed per lane.
+  constexpr int CPR = kBatchStageSB * (SB + SB2) / 16;
+  constexpr int JN = kBatchRows * CPR / 32;
+  static_assert(kBatchRows * CPR % 32 == 0, "whole chunks per lane");
   const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
-  const uint8_t* gi1 = a.W + p_lo * a.row_bytes + static_cast<int64_t>(wk) * kBatchColSB * SB + 16 * lane;
-  const uint8_t* gi2 =
-      kIsNVFP4 ? a.W2 + p_lo * a.row_bytes2 + static_cast<int64_t>(wk) * kBatchColSB * SB2 + 16 * lane : a.W;
-  const int nst = (nrows + kBatchRows - 1) / kBatchRows, nfull = nrows / kBatchRows;
-  const int tail = nrows - nfull * kBatchRows;
-  auto copy_row = [&](uint32_t d, const uint8_t* s1, const uint8_t* s2) {
+  uint32_t coff[JN], doff[JN], crow[JN], csb[JN], c2[JN];
 #pragma unroll
-    for (int j = 0; j < J1; ++j) {
-      switch (j) {
-        case 0: cp_async16_if<0, 0>(d, s1, ok1[j]); break;
-        case 1: cp_async16_if<512, 512>(d, s1, ok1[j]); break;
-        case 2: cp_async16_if<1024, 1024>(d, s1, ok1[j]); break;
-        case 3: cp_async16_if<1536, 1536>(d, s1, ok1[j]); break;
-        case 4: cp_async16_if<2048, 2048>(d, s1, ok1[j]); break;
-      }
-    }
-    if constexpr (kIsNVFP4) {
-#pragma unroll
-      for (int j = 0; j < J2; ++j) cp_async16_if<kBatchColSB * SB, 0>(d + 512 * j, s2 + 512 * j, ok2[j]);
-    }
-  };
+  for (int j = 0; j < JN; ++j) {
+    const int q = lane + 32 * j, row = q / CPR, off = q % CPR;
+    const bool two = kIsNVFP4 && off >= kBatchStageSB * SB / 16;
+    const int o2 = off - kBatchStageSB * SB / 16;
+    coff[j] = two ? row * rb2 + o2 * 16 : row * rb1 + off * 16;
+    csb[j] = two ? o2 : (off * 16) / SB;
+    crow[j] = row;
+    c2[j] = two;
+    doff[j] = row * SLICE + off * 16;
+  }
+  const int ntiles = (nrows + kBatchRows - 1) / kBatchRows;
+  const int spt = (ncols + kBatchStageSB - 1) / kBatchStageSB;  // stages per tile
+  const int nst = ntiles * spt;
   auto issue = [&](int st, uint32_t slot_sa) {
-    const uint32_t d = slot_sa + 16 * lane;
-    if (st < nfull) {
+    if (st < nst) {
+      const int tile = st / spt, h = st - tile * spt;
+      const int trows = min(kBatchRows, nrows - tile * kBatchRows);
+      const int64_t r0 = p_lo + tile * kBatchRows;
+      const int sb0 = kBatchColSB * wk + kBatchStageSB * h;  // first superblock of the stage in the row
+      const uint8_t* base1 = a.W + r0 * a.row_bytes + static_cast<int64_t>(sb0) * SB;
+      const uint8_t* base2 = kIsNVFP4 ? a.W2 + r0 * a.row_bytes2 + static_cast<int64_t>(sb0) * SB2 : base1;
+      const int nsb_left = ncols - kBatchStageSB * h;
 #pragma unroll
-      for (int r = 0; r < kBatchRows; ++r) copy_row(d + r * SLICE, gi1 + r * rb1, gi2 + r * rb2);
-      gi1 += kBatchRows * rb1;
-      gi2 += kBatchRows * rb2;
-    } else if (st < nst) {
-      for (int r = 0; r < tail; ++r) copy_row(d + r * SLICE, gi1 + r * rb1, gi2 + r * rb2);
+      for (int j = 0; j < JN; ++j) {
+        const uint32_t ok = (static_cast<int>(crow[j]) < trows) & (static_cast<int>(csb[j]) < nsb_left);
+        cp_async16_if<0, 0>(slot_sa + doff[j], (c2[j] ? base2 : base1) + coff[j], ok);
+      }
     }
     cp_async_commit();
   };
-  static_assert(J1 <= 5 && J2 <= 1, "row slice of at most 160 16-byte chunks");
 
   // Weight stages first (they do not depend on the previous kernel), then x.
 #pragma unroll 1
@@ -406,44 +403,52 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     osc1 = p2(-reinterpret_cast<const int*>(vscale)[2 * t4 + 1]);
   }
 
-  // ---- main loop: 16 rows per stage, every superblock of the K-column.
+  // ---- main loop: tiles of 16 rows, in stages of 2 superblocks.
   float* const out = a.Wk == 1 ? a.y + p_lo : a.ws + (static_cast<int64_t>(wk) * a.M) * a.N + p_lo;
   const int v0 = 2 * t4, v1 = 2 * t4 + 1;  // this lane's vectors
   uint32_t magic;  // fp16 (1024, 1024): the exponent under which two nibbles become fp16
   asm("mov.b32 %0, 0x64006400;" : "=r"(magic));
   uint32_t cs = ring_sa, is = ring_sa + (D - 1) * STAGE;
   const uint32_t xa_lane = xa_sa + lane * 8, xs_lane = xs_sa + lane * 8;
+  float y[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, v0), (row g, v1), (row g + 8, v0), (row g + 8, v1)
+  float dq[2][4] = {};                 // NVFP4: the tile's accumulator chains
   for (int st = 0; st < nst; ++st) {
     issue(st + D - 1, is);
     cp_async_wait<D - 1>();
     __syncwarp();
-    float y[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, v0), (row g, v1), (row g + 8, v0), (row g + 8, v1)
+    const int tile = st / spt, h = st - tile * spt;
     const uint32_t rg = cs + g * SLICE, r8 = cs + (g + 8) * SLICE;
-    if constexpr (!kIsNVFP4) {
 #pragma unroll
-      for (int c = 0; c < kBatchColSB; ++c)
-        if (c < ncols)
-          BatchQ4K::superblock(rg + SB * c, r8 + SB * c, t4, xa_lane + c * 16 * 256, xs_lane + c * 256, magic, y);
-    } else {
-      float dq[2][4] = {};
-#pragma unroll
-      for (int c = 0; c < kBatchColSB; ++c)
-        if (c < ncols)
-          BatchNVFP4::superblock(rg + SB * c, r8 + SB * c, rg + kBatchColSB * SB + SB2 * c,
-                               r8 + kBatchColSB * SB + SB2 * c, t4, xa_lane + c * 16 * 256, dq);
-      y[0] = (dq[0][0] + dq[1][0]) * osc0;
-      y[1] = (dq[0][1] + dq[1][1]) * osc1;
-      y[2] = (dq[0][2] + dq[1][2]) * osc0;
-      y[3] = (dq[0][3] + dq[1][3]) * osc1;
+    for (int c = 0; c < kBatchStageSB; ++c) {
+      const int sbk = kBatchStageSB * h + c;  // superblock within the K-column
+      if (sbk < ncols) {
+        if constexpr (!kIsNVFP4)
+          BatchQ4K::superblock(rg + SB * c, r8 + SB * c, t4, xa_lane + sbk * 16 * 256, xs_lane + sbk * 256, magic, y);
+        else
+          BatchNVFP4::superblock(rg + SB * c, r8 + SB * c, rg + kBatchStageSB * SB + SB2 * c,
+                                 r8 + kBatchStageSB * SB + SB2 * c, t4, xa_lane + sbk * 16 * 256, dq);
+      }
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
     is = cs;
     cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;
-    const int r0 = st * kBatchRows + g, r1 = r0 + 8;
-    if (v0 < a.M && r0 < nrows) out[static_cast<int64_t>(v0) * a.N + r0] = y[0];
-    if (v1 < a.M && r0 < nrows) out[static_cast<int64_t>(v1) * a.N + r0] = y[1];
-    if (v0 < a.M && r1 < nrows) out[static_cast<int64_t>(v0) * a.N + r1] = y[2];
-    if (v1 < a.M && r1 < nrows) out[static_cast<int64_t>(v1) * a.N + r1] = y[3];
+    if (h == spt - 1) {  // the tile's last stage: its sums are complete
+      if constexpr (kIsNVFP4) {
+        y[0] = (dq[0][0] + dq[1][0]) * osc0;
+        y[1] = (dq[0][1] + dq[1][1]) * osc1;
+        y[2] = (dq[0][2] + dq[1][2]) * osc0;
+        y[3] = (dq[0][3] + dq[1][3]) * osc1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dq[0][u] = dq[1][u] = 0.f;
+      }
+      const int r0 = tile * kBatchRows + g, r1 = r0 + 8;
+      if (v0 < a.M && r0 < nrows) out[static_cast<int64_t>(v0) * a.N + r0] = y[0];
+      if (v1 < a.M && r0 < nrows) out[static_cast<int64_t>(v1) * a.N + r0] = y[1];
+      if (v0 < a.M && r1 < nrows) out[static_cast<int64_t>(v0) * a.N + r1] = y[2];
+      if (v1 < a.M && r1 < nrows) out[static_cast<int64_t>(v1) * a.N + r1] = y[3];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) y[u] = 0.f;
+    }
   }
   cp_async_wait<0>();
 
