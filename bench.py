@@ -84,11 +84,12 @@ def launch_units(workload: str, gemvs):
     return units
 
 
-def unit_bytes(gemvs, idx, swiglu: bool) -> int:
-    """Algorithmic bytes of one launch: packed weights, x once, the outputs (fp32)."""
+def unit_bytes(gemvs, idx, swiglu: bool, batch: int = 1) -> int:
+    """Algorithmic bytes of one launch: packed weights once, x once per vector, the outputs
+    (fp32) of every vector."""
     K = gemvs[idx[0]][3]
     outs = gemvs[idx[0]][2] if swiglu else sum(gemvs[i][2] for i in idx)
-    return sum(synth.packed_bytes(gemvs[i][1], gemvs[i][2], gemvs[i][3]) for i in idx) + 2 * K + 4 * outs
+    return sum(synth.packed_bytes(gemvs[i][1], gemvs[i][2], gemvs[i][3]) for i in idx) + batch * (2 * K + 4 * outs)
 
 
 def gemv_bytes(fmt, N, K) -> int:
@@ -162,10 +163,11 @@ class Clocks:
 class OracleSampler:
     """Times the CPU oracle on row samples of every GEMV of a workload (host cores)."""
 
-    def __init__(self, gemvs, threads: int, seed: int = 0):
+    def __init__(self, gemvs, threads: int, seed: int = 0, batch: int = 1):
         import oracle
         self.oracle = oracle
         self.threads = threads
+        self.batch = batch  # activation vectors per GEMV (the oracle runs each one)
         self.pool = cf.ThreadPoolExecutor(max_workers=threads)  # the C oracle releases the GIL
         self.data = []
         for label, fmt, N, K, _ in gemvs:
@@ -175,7 +177,7 @@ class OracleSampler:
             t0 = time.perf_counter()
             oracle.gemv(fmt, x, W, N, K, 0, 4)
             per_row.append((time.perf_counter() - t0) / 4)
-        self.row_cost = sum(per_row)  # seconds for one row of every GEMV
+        self.row_cost = batch * sum(per_row)  # seconds for one row of every GEMV and vector
 
     def run(self, budget_s: float):
         """One timed sample costing about `budget_s` of wall time.  Returns (GB/s, s, text)."""
@@ -185,9 +187,10 @@ class OracleSampler:
             r = min(rows, N)
             start = (N - r) // 2
             chunk = max(1, math.ceil(r / self.threads))
-            for a in range(start, start + r, chunk):
-                jobs.append((fmt, x, W, N, K, a, min(start + r, a + chunk)))
-            nbytes += synth.packed_bytes(fmt, r, K) + 2 * K + 4 * r
+            for _ in range(self.batch):
+                for a in range(start, start + r, chunk):
+                    jobs.append((fmt, x, W, N, K, a, min(start + r, a + chunk)))
+            nbytes += synth.packed_bytes(fmt, r, K) + self.batch * (2 * K + 4 * r)
         t0 = time.perf_counter()
         list(self.pool.map(lambda j: self.oracle.gemv(*j), jobs))
         dt = time.perf_counter() - t0
@@ -203,7 +206,7 @@ def run_reference(args, gemvs, rank, world):
     if rank != 0:
         return 0
     threads = os.cpu_count() or 1
-    sampler = OracleSampler(gemvs, threads)
+    sampler = OracleSampler(gemvs, threads, batch=args.batch)
     per_step = max(0.01, 5.0 * args.cpu_seconds / max(1, args.steps + args.warmup))  # about a minute in all
     for _ in range(args.warmup):
         sampler.run(per_step)
@@ -218,7 +221,7 @@ def run_reference(args, gemvs, rank, world):
             "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "shapes": [f"{g[0]}:{synth.FORMAT_NAMES[g[1]]}:{g[2]}x{g[3]}"
-                                                             for g in gemvs]},
+                                                             for g in gemvs], "batch": args.batch},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"per step: {sample}"},
@@ -318,23 +321,24 @@ def run_ours(args, gemvs, rank, world):
     step_w_bytes = sum(synth.packed_bytes(f, n, k) for _, f, n, k, _ in gemvs)
     copies = max(2, math.ceil(3 * l2 / step_w_bytes))
     xs, Ws, ys, xbits = {}, [], [], {}
+    B = args.batch  # activation vectors per GEMV
     for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
         seed = synth.config_seed(1, gi) + 100 * rank
         W = synth.make_weights(fmt, N, K, seed)
         Wd = torch.from_numpy(W).to(dev)
         Ws.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
         if (xk, K, fmt) not in xs:
-            xb = synth.make_x(fmt, K, seed)
+            xb = np.stack([synth.make_x(fmt, K, seed + 7919 * m) for m in range(B)])  # [B, K]
             xbits[(xk, K, fmt)] = xb
             xs[(xk, K, fmt)] = torch.from_numpy(xb.view(np.int16).copy()).to(dev)
-        ys.append(torch.empty(N, dtype=torch.float32, device=dev))
+        ys.append(torch.empty((B, N), dtype=torch.float32, device=dev))
         del W
     units = launch_units(args.workload, gemvs)
     grouped = set(GROUPS.get(args.workload, {}).values())
     for label, idx, sw in units:
         if sw:
             ys[idx[1]] = None  # the up matrix of a SwiGLU pair has no output of its own
-    step_bytes = sum(unit_bytes(gemvs, idx, sw) for _, idx, sw in units)
+    step_bytes = sum(unit_bytes(gemvs, idx, sw, B) for _, idx, sw in units)
     stream = torch.cuda.Stream(device=dev)
 
     def launch(ui, c, s):
@@ -342,7 +346,9 @@ def run_ours(args, gemvs, rank, world):
         label, idx, sw = units[ui]
         _, fmt, N, K, xk = gemvs[idx[0]]
         x = xs[(xk, K, fmt)]
-        if label not in grouped:
+        if label not in grouped and B > 1:
+            qgemv.run_batch(h, fmt, x, B, Ws[idx[0]][c], N, K, ys[idx[0]], stream=s)
+        elif label not in grouped:
             qgemv.run(h, fmt, x, Ws[idx[0]][c], N, K, ys[idx[0]], stream=s)
         elif sw:
             qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[idx[0]][c], N, ys[idx[0]], packed_W_up=Ws[idx[1]][c],
@@ -425,17 +431,18 @@ def run_ours(args, gemvs, rank, world):
             samples.append(a.elapsed_time(b) * 1e3 / R)
         us = statistics.median(samples)
         shape = " + ".join(f"{synth.FORMAT_NAMES[gemvs[i][1]]} {gemvs[i][2]}x{gemvs[i][3]}" for i in idx)
-        per_call[label] = {"us": us, "GB/s": unit_bytes(gemvs, idx, sw) / (us * 1e-6) / 1e9,
+        per_call[label] = {"us": us, "GB/s": unit_bytes(gemvs, idx, sw, B) / (us * 1e-6) / 1e9,
                            "shape": shape + (" (SwiGLU pair)" if sw else "")}
         if label not in grouped:
             per_call[label]["plan"] = qgemv.describe(h, gemvs[idx[0]][1], gemvs[idx[0]][2], gemvs[idx[0]][3])
         del gg
-    dom = max(units, key=lambda u_: unit_bytes(gemvs, u_[1], u_[2]))[0]
+    dom = max(units, key=lambda u_: unit_bytes(gemvs, u_[1], u_[2], B))[0]
     peak, peak_kind = load_peaks()
     achieved = per_call[dom]["GB/s"]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": args.traffic,
-                "kernel": f"{'group_kernel' if dom in grouped else 'stream_kernel'} {per_call[dom]['shape']}",
+                "kernel": f"{'group_kernel' if dom in grouped else 'batch_kernel' if B > 1 else 'stream_kernel'} "
+                          f"{per_call[dom]['shape']}" + (f" x {B} vectors" if B > 1 else ""),
                 "peak_kind": f"hbm_gbs of {peak_kind} (copy bandwidth)",
                 "achieved_how": "algorithmic bytes per launch / mean launch duration over graph replays of 200 "
                                 "launches rotating weight copies (CUDA events on the launch stream)"}
@@ -444,8 +451,8 @@ def run_ours(args, gemvs, rank, world):
     e2e_steps = min(args.steps, 2000)
     hx = {k: torch.from_numpy(v.view(np.int16).copy()).pin_memory() for k, v in xbits.items()}
     outs = [y for y in ys if y is not None]
-    hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in outs]
-    h2d = sum(2 * k[1] for k in hx)
+    hy = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in outs]
+    h2d = sum(2 * v.size for v in xbits.values())
     d2h = sum(4 * y.numel() for y in outs)
     with torch.cuda.stream(stream):
         for i in range(5):
@@ -476,7 +483,7 @@ def run_ours(args, gemvs, rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        sampler = OracleSampler(gemvs, threads)
+        sampler = OracleSampler(gemvs, threads, batch=B)
         rates, spent = [], 0.0
         while spent < args.cpu_seconds or len(rates) < 3:  # repeated bounded samples, median rate
             rate, dt, sample = sampler.run(max(0.5, args.cpu_seconds / 5))
@@ -496,6 +503,7 @@ def run_ours(args, gemvs, rank, world):
                            "l2": f"inputs larger than L2: {copies} rotating weight copies = "
                                  f"{copies * step_w_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
                            "timing": f"CUDA graph of {spg} steps replayed {reps}x, CUDA events",
+                           "batch": B,
                            "launches": [f"{u_[0]}:{'+'.join(gemvs[i][0] for i in u_[1])}"
                                         + (":swiglu" if u_[2] else "") for u_ in units],
                            "pdl": bool(args.pdl)},
@@ -525,11 +533,17 @@ def main(argv=None):
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="only run this many plain launches of each GEMV (for a profiler) and exit")
     ap.add_argument("--only", default=None, help="with --profile-launches: the one GEMV label to run")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="activation vectors per GEMV (1..8; > 1 runs qgemv_run_batch, ungrouped workloads only)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, when known for this build")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not 1 <= args.batch <= 8:
+        ap.error("--batch must be in 1..8")
+    if args.batch > 1 and GROUPS.get(args.workload):
+        ap.error("--batch > 1 applies to workloads without grouped launches")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     gemvs = WORKLOADS[args.workload]

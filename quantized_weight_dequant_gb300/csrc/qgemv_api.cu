@@ -666,9 +666,10 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   const int f = static_cast<int>(fmt);
   int64_t rb1 = 0, rb2 = 0;
   const int64_t Wk = (K / 256 + kBatchColSB - 1) / kBatchColSB;
-  // The batch kernel: Q4_K / NVFP4 with streaming-eligible rows, its column sums in the
-  // workspace.  Otherwise each vector runs the single-vector path.
-  const bool batch = (f == F_Q4K || f == F_NVFP4) && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
+  // The batch kernel: two or more vectors, Q4_K / NVFP4 with streaming-eligible rows, its
+  // column sums in the workspace.  Otherwise each vector runs the single-vector path (which
+  // is also the faster one for a single vector).
+  const bool batch = M > 1 && (f == F_Q4K || f == F_NVFP4) && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
                      (Wk == 1 || static_cast<double>(M) * N * Wk <= static_cast<double>(kWsFloats));
   if (!batch) {
     for (int m = 0; m < M; ++m) {

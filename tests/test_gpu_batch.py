@@ -1,8 +1,8 @@
 """GPU parity of the small-batch GEMV (qgemv_run_batch): M = 1..8 activation vectors against
 the oracle, one vector at a time, each output within |y - y_ref| <= 2e-3 * sum|x w| + 1e-5
 of its own vector.  Q4_K and NVFP4 run the mma.sync kernel (one, two and seven K-columns,
-ragged row counts, partial last K-columns); the other formats run the single-vector path
-per vector."""
+ragged row counts, partial last K-columns) for M >= 2; M = 1 and the other formats run the
+single-vector path per vector."""
 import numpy as np
 import pytest
 import torch
