@@ -279,9 +279,15 @@ def run_profile_launches(args, gemvs):
             Ws.append(torch.from_numpy(synth.make_weights(fmt, N, K, synth.config_seed(1, gi))).cuda())
             ys.append(torch.empty(N, dtype=torch.float32, device="cuda"))
         _, fmt, N, K, _ = gemvs[idx[0]]
-        x = torch.from_numpy(synth.make_x(fmt, K, synth.config_seed(1, idx[0])).view(np.int16).copy()).cuda()
+        B = args.batch
+        x = torch.from_numpy(np.stack([synth.make_x(fmt, K, synth.config_seed(1, idx[0]) + 7919 * m)
+                                       for m in range(B)]).view(np.int16)).cuda()
+        if B > 1:
+            ys = [torch.empty((B, gemvs[gi][2]), dtype=torch.float32, device="cuda") for gi in idx]
         for _ in range(args.profile_launches):
-            if label not in grouped:
+            if label not in grouped and B > 1:
+                qgemv.run_batch(h, fmt, x, B, Ws[0], N, K, ys[0])
+            elif label not in grouped:
                 qgemv.run(h, fmt, x, Ws[0], N, K, ys[0])
             elif sw:
                 qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[0], N, ys[0], packed_W_up=Ws[1], swiglu=True)])
@@ -292,7 +298,7 @@ def run_profile_launches(args, gemvs):
         st = qgemv.check_error(h)
         if st != qgemv.OK:
             raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
-        plan = qgemv.describe(h, fmt, N, K) if label not in grouped else "grouped launch"
+        plan = (qgemv.describe(h, fmt, N, K) if B == 1 else f"batch of {B}") if label not in grouped else "grouped launch"
         print(f"{label}: {args.profile_launches} launches, {plan}", flush=True)
     h.close()
     return 0
