@@ -248,10 +248,10 @@ qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x,
 /* ---------------------------------------------------------------- small batches
  * Y = X . dequant(W)^T for M = 1..QGEMV_MAX_BATCH activation vectors at once (the general
  * GEMV of the Q4_K page, "What is a GEMV", with x of shape (M, K) instead of (1, K)): every
- * packed weight is read and decoded once and serves all M vectors.  For M >= 2, Q4_K and
- * NVFP4 with K a multiple of 256 use the tensor cores' mma.sync path (decoded weights go
- * straight into the A fragments; the M vectors fill the B operand), as long as
- * M * N * ceil(K / 1024) fits the handle's workspace (4 Mi column sums); M = 1, other formats
+ * packed weight is read and decoded once and serves all M vectors.  For M >= 2, Q4_K, Q5_K,
+ * Q8_0 and NVFP4 with K a multiple of 256 use the tensor cores' mma.sync path (decoded weights
+ * go straight into the A fragments; the M vectors fill the B operand), as long as
+ * M * N * ceil(K / 1024) fits the handle's workspace (4 Mi column sums); M = 1, Q6_K, TQ1_0
  * and other shapes run the single-vector path once per vector. */
 #define QGEMV_MAX_BATCH 8
 

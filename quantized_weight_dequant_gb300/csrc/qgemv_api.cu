@@ -38,7 +38,7 @@ struct Handle {
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
   size_t group1_smem_max[6][2][2][3] = {};  // one-format grouped kernels [format][pairs][R 2/4][D 2/3/4]
-  size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3] (Q4_K, NVFP4)
+  size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3] (Q4_K, Q5_K, Q8_0, NVFP4)
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -554,7 +554,7 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
             return QGEMV_ERR_CUDA;
           }
         }
-  for (int f : {static_cast<int>(F_Q4K), static_cast<int>(F_NVFP4)})
+  for (int f : {static_cast<int>(F_Q4K), static_cast<int>(F_Q5K), static_cast<int>(F_Q80), static_cast<int>(F_NVFP4)})
     for (int D : {2, 3}) {
       cudaFuncAttributes fa;
       const void* fn = batch_kernel_for(f, D);
@@ -669,7 +669,12 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   // The batch kernel: two or more vectors, Q4_K / NVFP4 with streaming-eligible rows, its
   // column sums in the workspace.  Otherwise each vector runs the single-vector path (which
   // is also the faster one for a single vector).
-  const bool batch = M > 1 && (f == F_Q4K || f == F_NVFP4) && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
+  const int warps = kBatchThreads / 32;
+  const bool fmt_ok_b = f == F_Q4K || f == F_Q5K || f == F_Q80 || f == F_NVFP4;
+  int D = 3;
+  while (fmt_ok_b && D > 2 && batch_smem_bytes(f, warps, D) > h->batch_smem_max[f][D - 2]) --D;
+  const bool batch = M > 1 && fmt_ok_b && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
+                     batch_smem_bytes(f, warps, D) <= h->batch_smem_max[f][D - 2] &&
                      (Wk == 1 || static_cast<double>(M) * N * Wk <= static_cast<double>(kWsFloats));
   if (!batch) {
     for (int m = 0; m < M; ++m) {
@@ -678,15 +683,11 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
     }
     return QGEMV_OK;
   }
-  const int warps = kBatchThreads / 32;
   int64_t ranges = std::max<int64_t>(1, h->sms / Wk);
   ranges = std::min<int64_t>(ranges, (N + kBatchRows - 1) / kBatchRows);
   ranges = std::max<int64_t>(1, std::min<int64_t>(ranges, kMaxRanges));
   if (N / ranges >= 0x7ffffffe) return QGEMV_ERR_BAD_SHAPE;
-  int D = 3;
-  while (D > 2 && batch_smem_bytes(f, warps, D) > h->batch_smem_max[f][D - 2]) --D;
   const size_t smem = batch_smem_bytes(f, warps, D);
-  if (smem > h->batch_smem_max[f][D - 2]) return QGEMV_ERR_BAD_SHAPE;
   BatchArgs a{};
   a.W = static_cast<const uint8_t*>(W);
   a.W2 = (f == F_NVFP4) ? a.W + N * (K / 2) : nullptr;

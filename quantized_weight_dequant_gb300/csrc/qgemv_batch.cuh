@@ -42,7 +42,7 @@ namespace qg {
 constexpr int kBatchMax = 8;        // activation vectors (the MMA's N)
 constexpr int kBatchRows = 16;      // weight rows per stage (the MMA's M)
 constexpr int kBatchColSB = 4;      // superblocks per K-column
-constexpr int kBatchStageSB = 2;    // superblocks per stage (a tile of 16 rows takes 1 or 2)
+constexpr int kBatchStageSB = 2;    // superblocks per stage by default (a 16-row tile takes 1 or 2)
 constexpr int kBatchThreads = 512;  // 16 warps per CTA
 
 struct BatchArgs {
@@ -129,8 +129,16 @@ __device__ __forceinline__ uint32_t int2_to_h2(uint32_t lo, uint32_t hi) {
 }
 
 // ----------------------------------------------------------------------------- Q4_K
+// Decoders.  Each has kSB / kSB2 (bytes of a superblock in stream 1 / 2); kMinTerm (a group
+// minimum term, taken through the staged group sums of x); kFolded (every scale folded into A,
+// so the accumulators run over a whole tile; otherwise the superblock scales d, dmin are
+// applied to each superblock's sums); kBF16 (x is bf16, staged as scaled fp16); chunk_slot
+// (where an aligned chunk of 4 x values goes in the fragment buffer); and superblock (one
+// superblock c of a stage, rows g and g + 8 from the row slots at rg / r8).
 struct BatchQ4K {
   static constexpr int kSB = 144, kSB2 = 0;
+  static constexpr int kStageSB = kBatchStageSB, kPad = 16;  // superblocks per stage, slot padding
+  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false;
 
   // x chunk of 4 fp16 values (elements e..e+3 of a superblock, e % 4 == 0) -> its slot in the
   // fragment buffer: k-step s and lane t4 part.  Byte j of chunk t4 holds element 64 t4 + j
@@ -164,10 +172,10 @@ struct BatchQ4K {
     Mn = int2_to_h2(ml, mh);
   }
 
-  // Lane (g, t4): the superblock at shared addresses `bg` (row g) and `b8` (row g + 8); xa / xs
-  // its fragment addresses.  Adds the superblock's contribution to the lane's four sums.
-  __device__ __forceinline__ static void superblock(uint32_t bg, uint32_t b8, int t4, uint32_t xa, uint32_t xs,
+  // Lane (g, t4): adds the superblock's contribution to the lane's four sums y.
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t xs,
                                                     uint32_t magic, float (&y)[4]) {
+    const uint32_t bg = rg + kSB * c, b8 = r8 + kSB * c;
     const uint4 hg = lds_v4(bg), h8 = lds_v4(b8);
     const uint4 g0 = lds_v4(bg + 16 + 32 * t4), g1 = lds_v4(bg + 32 + 32 * t4);
     const uint4 e0 = lds_v4(b8 + 16 + 32 * t4), e1 = lds_v4(b8 + 32 + 32 * t4);
@@ -211,6 +219,8 @@ struct BatchQ4K {
 // ----------------------------------------------------------------------------- NVFP4
 struct BatchNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
+  static constexpr int kStageSB = kBatchStageSB, kPad = 16;
+  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = true;
 
   // Chunk t4 of a superblock is nibble bytes [32 t4, 32 t4 + 32) = elements 64 t4 + [0, 64);
   // word i (elements 64 t4 + 8 i + [0, 8)) feeds steps 2 i (elements +0..3) and 2 i + 1
@@ -221,9 +231,11 @@ struct BatchNVFP4 {
     v = raw;
   }
 
-  // Rows g (nibbles at ng, scales at sg) and g + 8 (n8, s8) of a superblock.
-  __device__ __forceinline__ static void superblock(uint32_t ng, uint32_t n8, uint32_t sg, uint32_t s8, int t4,
-                                                    uint32_t xa, float (&dq)[2][4]) {
+  // Nibbles of superblock c at 128 c of a row slot, its scales at 2 * 128 + 16 c.
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t,
+                                                    uint32_t, float (&dq)[2][4]) {
+    const uint32_t ng = rg + kSB * c, n8 = r8 + kSB * c;
+    const uint32_t sg = rg + kStageSB * kSB + kSB2 * c, s8 = r8 + kStageSB * kSB + kSB2 * c;
     const uint4 g0 = lds_v4(ng + 32 * t4), g1 = lds_v4(ng + 32 * t4 + 16);
     const uint4 e0 = lds_v4(n8 + 32 * t4), e1 = lds_v4(n8 + 32 * t4 + 16);
     const uint32_t sG = lds_u32(sg + 4 * t4) & 0x7F7F7F7Fu;  // |scale| of blocks 4 t4 .. 4 t4 + 3
@@ -248,11 +260,131 @@ struct BatchNVFP4 {
   }
 };
 
-// Bytes of one row slot in a ring stage: the row's 2 superblocks (stream 1, then stream 2)
-// plus 16 bytes, so that the 16 rows of a stage start in different shared-memory banks.
+// ----------------------------------------------------------------------------- Q5_K
+// The Q4_K layout with a fifth bit per code: qh[32] at 16, quants at 48.  Codes (q5 <= 31)
+// times the 6-bit group scale stay exact fp16 integers (<= 1953).
+struct BatchQ5K {
+  static constexpr int kSB = 176, kSB2 = 0;
+  static constexpr int kStageSB = kBatchStageSB, kPad = 16;
+  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false;
+
+  __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
+    BatchQ4K::chunk_slot(e, step, t4, v, raw);
+  }
+
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t xs,
+                                                    uint32_t magic, float (&y)[4]) {
+    const uint32_t bg = rg + kSB * c, b8 = r8 + kSB * c;
+    const uint4 hg = lds_v4(bg), h8 = lds_v4(b8);
+    const uint4 g0 = lds_v4(bg + 48 + 32 * t4), g1 = lds_v4(bg + 64 + 32 * t4);
+    const uint4 e0 = lds_v4(b8 + 48 + 32 * t4), e1 = lds_v4(b8 + 64 + 32 * t4);
+    const uint4 qg0 = lds_v4(bg + 16), qg1 = lds_v4(bg + 32);  // qh[0..32) of row g
+    const uint4 q80 = lds_v4(b8 + 16), q81 = lds_v4(b8 + 32);
+    uint32_t Sg, Mg, S8, M8;
+    BatchQ4K::group_scales(hg, t4, Sg, Mg);
+    BatchQ4K::group_scales(h8, t4, S8, M8);
+    // both planes: (1024 + q5) s - 1024 s
+    const uint32_t SLg = __byte_perm(Sg, Sg, 0x1010), SL8 = __byte_perm(S8, S8, 0x1010);
+    const uint32_t SHg = __byte_perm(Sg, Sg, 0x3232), SH8 = __byte_perm(S8, S8, 0x3232);
+    const uint32_t CLg = hmul2_u(SLg, 0xE400E400u), CL8 = hmul2_u(SL8, 0xE400E400u);
+    const uint32_t CHg = hmul2_u(SHg, 0xE400E400u), CH8 = hmul2_u(SH8, 0xE400E400u);
+    const uint32_t wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t w8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    const uint32_t hqg[8] = {qg0.x, qg0.y, qg0.z, qg0.w, qg1.x, qg1.y, qg1.z, qg1.w};
+    const uint32_t hq8[8] = {q80.x, q80.y, q80.z, q80.w, q81.x, q81.y, q81.z, q81.w};
+    const uint32_t sh = 2u * t4;  // qh bit 2 t4 (low nibbles) and 2 t4 + 1 (high nibbles)
+    float dq[2][4] = {};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // 5-bit codes of the word's four bytes, low- and high-nibble planes
+      const uint32_t hg_ = hqg[i] >> sh, h8_ = hq8[i] >> sh;
+      const uint32_t lg = and_or<0x0F0F0F0Fu>(wg[i], (hg_ << 4) & 0x10101010u);
+      const uint32_t ug = and_or<0x0F0F0F0Fu>(wg[i] >> 4, (hg_ << 3) & 0x10101010u);
+      const uint32_t l8 = and_or<0x0F0F0F0Fu>(w8[i], (h8_ << 4) & 0x10101010u);
+      const uint32_t u8 = and_or<0x0F0F0F0Fu>(w8[i] >> 4, (h8_ << 3) & 0x10101010u);
+      const uint2 xl = lds_v2(xa + (2 * i) * 256), xh = lds_v2(xa + (2 * i + 1) * 256);
+      mma16816(dq[0], hfma2_u(and_or<0x001F001Fu>(lg, magic), SLg, CLg),
+               hfma2_u(and_or<0x001F001Fu>(l8, magic), SL8, CL8),
+               hfma2_u(and_or<0x001F001Fu>(lg >> 8, magic), SLg, CLg),
+               hfma2_u(and_or<0x001F001Fu>(l8 >> 8, magic), SL8, CL8), xl.x, xl.y);
+      mma16816(dq[1], hfma2_u(and_or<0x001F001Fu>(ug, magic), SHg, CHg),
+               hfma2_u(and_or<0x001F001Fu>(u8, magic), SH8, CH8),
+               hfma2_u(and_or<0x001F001Fu>(ug >> 8, magic), SHg, CHg),
+               hfma2_u(and_or<0x001F001Fu>(u8 >> 8, magic), SH8, CH8), xh.x, xh.y);
+    }
+    float dm[4] = {};
+    const uint2 X = lds_v2(xs);
+    mma1688(dm, Mg, M8, X.x);
+    mma1688(dm, Mg, M8, X.y);
+    const float dg = h2f(hg.x), mg = h2f(hg.x >> 16) * 64.f, d8 = h2f(h8.x), m8 = h2f(h8.x >> 16) * 64.f;
+    y[0] += fmaf(dg, dq[0][0] + dq[1][0], -mg * dm[0]);
+    y[1] += fmaf(dg, dq[0][1] + dq[1][1], -mg * dm[1]);
+    y[2] += fmaf(d8, dq[0][2] + dq[1][2], -m8 * dm[2]);
+    y[3] += fmaf(d8, dq[0][3] + dq[1][3], -m8 * dm[3]);
+  }
+};
+
+// ----------------------------------------------------------------------------- Q8_0
+// A superblock is 8 blocks of 34 bytes (d, then 32 int8 codes).  Lane t4 takes blocks 2 t4 and
+// 2 t4 + 1 (bytes [68 t4, 68 t4 + 68), read as 17 aligned words), one word of 4 codes per
+// k-step.  A = d * q rounded once to fp16 (the block scale differs between the lanes of a
+// k-step, so it cannot wait for the accumulator): a relative error of at most 2^-11 per
+// weight, a quarter of the GEMV bound.
+struct BatchQ80 {
+  static constexpr int kSB = 272, kSB2 = 0;
+  // one superblock per stage (two would not fit 16 warps x 2 stages), slots padded by 32 so
+  // the word loads of the 8 rows g fall in different banks
+  static constexpr int kStageSB = 1, kPad = 32;
+  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = false;
+
+  // elements 64 t4 + 4 s + (0..3): pairs (x0, x2) and (x1, x3), as bytes (b0, b2), (b1, b3)
+  __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
+    t4 = e >> 6;
+    step = (e & 63) >> 2;
+    v.x = __byte_perm(raw.x, raw.y, 0x5410);
+    v.y = __byte_perm(raw.x, raw.y, 0x7632);
+  }
+
+  // The lane's two blocks of one row: 17 aligned words from `base` (68 t4 into the superblock).
+  // Block 2 t4: d in bytes 0..1, codes in bytes 2..33 (unaligned: one PRMT per word); block
+  // 2 t4 + 1: d in bytes 34..35, codes in bytes 36..67 (aligned).
+  __device__ __forceinline__ static void lane_blocks(uint32_t base, uint32_t (&q)[16], uint32_t& dA, uint32_t& dB) {
+    uint32_t w[17];
+#pragma unroll
+    for (int k = 0; k < 17; ++k) w[k] = lds_u32(base + 4 * k);
+    dA = __byte_perm(w[0], w[0], 0x1010);
+    dB = __byte_perm(w[8], w[8], 0x3232);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      q[k] = __byte_perm(w[k], w[k + 1], 0x5432);
+      q[8 + k] = w[9 + k];
+    }
+  }
+
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t,
+                                                    uint32_t magic, float (&dq)[2][4]) {
+    uint32_t qg[16], q8[16], dAg, dBg, dA8, dB8;
+    lane_blocks(rg + kSB * c + 68 * t4, qg, dAg, dBg);
+    lane_blocks(r8 + kSB * c + 68 * t4, q8, dA8, dB8);
+    const uint32_t off = 0x64806480u;  // fp16 (1152, 1152) = 1024 + 128
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const uint32_t dg = s < 8 ? dAg : dBg, d8 = s < 8 ? dA8 : dB8;
+      const uint32_t ug = qg[s] ^ 0x80808080u, u8 = q8[s] ^ 0x80808080u;  // q + 128 per byte
+      const uint2 xs_ = lds_v2(xa + s * 256);
+      mma16816(dq[s & 1], hmul2_u(hsub2_u(and_or<0x00FF00FFu>(ug, magic), off), dg),
+               hmul2_u(hsub2_u(and_or<0x00FF00FFu>(u8, magic), off), d8),
+               hmul2_u(hsub2_u(and_or<0x00FF00FFu>(ug >> 8, magic), off), dg),
+               hmul2_u(hsub2_u(and_or<0x00FF00FFu>(u8 >> 8, magic), off), d8), xs_.x, xs_.y);
+    }
+  }
+};
+
+// Bytes of one row slot in a ring stage: the row's superblocks of the stage (stream 1, then
+// stream 2) plus padding, so that the 16 rows of a stage start in different shared-memory banks.
 template <class Fmt>
 __host__ __device__ constexpr int batch_slice() {
-  return kBatchStageSB * (Fmt::kSB + Fmt::kSB2) + 16;
+  return Fmt::kStageSB * (Fmt::kSB + Fmt::kSB2) + Fmt::kPad;
 }
 
 template <class Fmt, int D>
@@ -260,7 +392,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = Fmt::kSB, SB2 = Fmt::kSB2, SLICE = batch_slice<Fmt>();
   constexpr int STAGE = kBatchRows * SLICE;
-  constexpr bool kIsNVFP4 = SB2 > 0;
+  constexpr bool kTwo = SB2 > 0;  // a second stream (NVFP4 scales)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   const unsigned uWk = static_cast<unsigned>(a.Wk);
@@ -281,34 +413,35 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
   // Copies.  A stage is 16 rows x CPR 16-byte chunks (2 superblocks of stream 1, then of
   // stream 2); lane l copies chunks l + 32 j, whose row, source offset (from the stage's row
   // block) and slot offset are fixed per lane.
-  constexpr int CPR = kBatchStageSB * (SB + SB2) / 16;
-  constexpr int JN = kBatchRows * CPR / 32;
-  static_assert(kBatchRows * CPR % 32 == 0, "whole chunks per lane");
+  constexpr int SSB = Fmt::kStageSB;
+  constexpr int CPR = SSB * (SB + SB2) / 16;
+  constexpr int NCH = kBatchRows * CPR;  // chunks per stage
+  constexpr int JN = (NCH + 31) / 32;
   const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
   uint32_t coff[JN], doff[JN], crow[JN], csb[JN], c2[JN];
 #pragma unroll
   for (int j = 0; j < JN; ++j) {
     const int q = lane + 32 * j, row = q / CPR, off = q % CPR;
-    const bool two = kIsNVFP4 && off >= kBatchStageSB * SB / 16;
-    const int o2 = off - kBatchStageSB * SB / 16;
+    const bool two = kTwo && off >= SSB * SB / 16;
+    const int o2 = off - SSB * SB / 16;
     coff[j] = two ? row * rb2 + o2 * 16 : row * rb1 + off * 16;
-    csb[j] = two ? o2 : (off * 16) / SB;
+    csb[j] = q < NCH ? (two ? o2 : (off * 16) / SB) : SSB;  // chunks past the stage: never copied
     crow[j] = row;
     c2[j] = two;
     doff[j] = row * SLICE + off * 16;
   }
   const int ntiles = (nrows + kBatchRows - 1) / kBatchRows;
-  const int spt = (ncols + kBatchStageSB - 1) / kBatchStageSB;  // stages per tile
+  const int spt = (ncols + SSB - 1) / SSB;  // stages per tile
   const int nst = ntiles * spt;
   auto issue = [&](int st, uint32_t slot_sa) {
     if (st < nst) {
       const int tile = st / spt, h = st - tile * spt;
       const int trows = min(kBatchRows, nrows - tile * kBatchRows);
       const int64_t r0 = p_lo + tile * kBatchRows;
-      const int sb0 = kBatchColSB * wk + kBatchStageSB * h;  // first superblock of the stage in the row
+      const int sb0 = kBatchColSB * wk + SSB * h;  // first superblock of the stage in the row
       const uint8_t* base1 = a.W + r0 * a.row_bytes + static_cast<int64_t>(sb0) * SB;
-      const uint8_t* base2 = kIsNVFP4 ? a.W2 + r0 * a.row_bytes2 + static_cast<int64_t>(sb0) * SB2 : base1;
-      const int nsb_left = ncols - kBatchStageSB * h;
+      const uint8_t* base2 = kTwo ? a.W2 + r0 * a.row_bytes2 + static_cast<int64_t>(sb0) * SB2 : base1;
+      const int nsb_left = ncols - SSB * h;
 #pragma unroll
       for (int j = 0; j < JN; ++j) {
         const uint32_t ok = (static_cast<int>(crow[j]) < trows) & (static_cast<int>(csb[j]) < nsb_left);
@@ -337,7 +470,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     if (v < a.M && (c >> 6) < ncols)
       raw[k] = __ldcg(reinterpret_cast<const uint2*>(a.x + static_cast<int64_t>(v) * a.K + kc0) + c);
   }
-  if constexpr (kIsNVFP4) {
+  if constexpr (Fmt::kBF16) {
     // per vector: sigma with max |x| * 2^sigma in [2^14, 2^15) over this K-column
     int* const vmax = reinterpret_cast<int*>(vscale);
     if (threadIdx.x < kBatchMax) vmax[threadIdx.x] = 0;
@@ -364,7 +497,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     const int idx = threadIdx.x + kBatchThreads * k, v = idx / kChunks, c = idx % kChunks;
     const int sb = c >> 6, e = 4 * (c & 63);
     uint2 r = raw[k];
-    if constexpr (kIsNVFP4) {
+    if constexpr (Fmt::kBF16) {
       const float f = p2(reinterpret_cast<const int*>(vscale)[v]);
       const __half2 h0 = __floats2half2_rn(bf2f(r.x) * f, bf2f(r.x >> 16) * f);
       const __half2 h1 = __floats2half2_rn(bf2f(r.y) * f, bf2f(r.y >> 16) * f);
@@ -375,7 +508,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     Fmt::chunk_slot(e, step, tq, val, r);
     const int ln = 4 * v + tq;
     *reinterpret_cast<uint2*>(smem + L.xa + ((sb * 16 + step) * 32 + ln) * 8) = val;
-    if constexpr (!kIsNVFP4) {
+    if constexpr (Fmt::kMinTerm) {
       // group sums of x (for the minimum term): 8 chunks of 4 make a group of 32
       float gs = __half2float(__ushort_as_half(static_cast<unsigned short>(r.x & 0xFFFFu))) +
                  __half2float(__ushort_as_half(static_cast<unsigned short>(r.x >> 16))) +
@@ -396,9 +529,9 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     }
   }
   __syncthreads();
-  // output scales of this lane's vectors 2 t4 and 2 t4 + 1 (NVFP4: 2^-sigma)
+  // output scales of this lane's vectors 2 t4 and 2 t4 + 1 (bf16 x: 2^-sigma)
   float osc0 = 1.f, osc1 = 1.f;
-  if constexpr (kIsNVFP4) {
+  if constexpr (Fmt::kBF16) {
     osc0 = p2(-reinterpret_cast<const int*>(vscale)[2 * t4]);
     osc1 = p2(-reinterpret_cast<const int*>(vscale)[2 * t4 + 1]);
   }
@@ -411,7 +544,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
   uint32_t cs = ring_sa, is = ring_sa + (D - 1) * STAGE;
   const uint32_t xa_lane = xa_sa + lane * 8, xs_lane = xs_sa + lane * 8;
   float y[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, v0), (row g, v1), (row g + 8, v0), (row g + 8, v1)
-  float dq[2][4] = {};                 // NVFP4: the tile's accumulator chains
+  float dq[2][4] = {};                 // folded scales: the tile's accumulator chains
   for (int st = 0; st < nst; ++st) {
     issue(st + D - 1, is);
     cp_async_wait<D - 1>();
@@ -419,21 +552,20 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     const int tile = st / spt, h = st - tile * spt;
     const uint32_t rg = cs + g * SLICE, r8 = cs + (g + 8) * SLICE;
 #pragma unroll
-    for (int c = 0; c < kBatchStageSB; ++c) {
-      const int sbk = kBatchStageSB * h + c;  // superblock within the K-column
+    for (int c = 0; c < SSB; ++c) {
+      const int sbk = SSB * h + c;  // superblock within the K-column
       if (sbk < ncols) {
-        if constexpr (!kIsNVFP4)
-          BatchQ4K::superblock(rg + SB * c, r8 + SB * c, t4, xa_lane + sbk * 16 * 256, xs_lane + sbk * 256, magic, y);
+        if constexpr (Fmt::kFolded)
+          Fmt::superblock(rg, r8, c, t4, xa_lane + sbk * 16 * 256, xs_lane + sbk * 256, magic, dq);
         else
-          BatchNVFP4::superblock(rg + SB * c, r8 + SB * c, rg + kBatchStageSB * SB + SB2 * c,
-                                 r8 + kBatchStageSB * SB + SB2 * c, t4, xa_lane + sbk * 16 * 256, dq);
+          Fmt::superblock(rg, r8, c, t4, xa_lane + sbk * 16 * 256, xs_lane + sbk * 256, magic, y);
       }
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
     is = cs;
     cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;
     if (h == spt - 1) {  // the tile's last stage: its sums are complete
-      if constexpr (kIsNVFP4) {
+      if constexpr (Fmt::kFolded) {
         y[0] = (dq[0][0] + dq[1][0]) * osc0;
         y[1] = (dq[0][1] + dq[1][1]) * osc1;
         y[2] = (dq[0][2] + dq[1][2]) * osc0;

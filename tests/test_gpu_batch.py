@@ -1,8 +1,8 @@
 """GPU parity of the small-batch GEMV (qgemv_run_batch): M = 1..8 activation vectors against
 the oracle, one vector at a time, each output within |y - y_ref| <= 2e-3 * sum|x w| + 1e-5
-of its own vector.  Q4_K and NVFP4 run the mma.sync kernel (one, two and seven K-columns,
-ragged row counts, partial last K-columns) for M >= 2; M = 1 and the other formats run the
-single-vector path per vector."""
+of its own vector.  Q4_K, Q5_K, Q8_0 and NVFP4 run the mma.sync kernel (one to fourteen
+K-columns, ragged row counts, partial last K-columns) for M >= 2; M = 1, Q6_K, TQ1_0 and
+shapes the streaming kernels do not take run the single-vector path per vector."""
 import numpy as np
 import pytest
 import torch
@@ -56,7 +56,8 @@ def _run(h, fmt, X, W_dev, N, K):
 
 SHAPES = [(synth.Q4_K, 77, 2048), (synth.Q4_K, 300, 4096), (synth.Q4_K, 129, 14336), (synth.Q4_K, 8, 2304),
           (synth.Q4_K, 1, 256), (synth.NVFP4, 65, 2048), (synth.NVFP4, 40, 14336), (synth.NVFP4, 333, 4352),
-          (synth.NVFP4, 3, 256)]
+          (synth.NVFP4, 3, 256), (synth.Q5_K, 77, 4096), (synth.Q5_K, 33, 12288), (synth.Q5_K, 5, 768),
+          (synth.Q8_0, 65, 4096), (synth.Q8_0, 40, 12288), (synth.Q8_0, 17, 1280)]
 
 
 @pytest.mark.parametrize("fmt,N,K", SHAPES)
@@ -71,7 +72,7 @@ def test_batch_matches_oracle(h, fmt, N, K, M):
 
 
 @pytest.mark.parametrize("fmt,N,K", [(synth.Q6_K, 40, 12288), (synth.TQ1_0, 33, 4096), (synth.Q8_0, 50, 4000),
-                                     (synth.Q5_K, 17, 2048), (synth.NVFP4, 9, 4016)])
+                                     (synth.Q6_K, 17, 2048), (synth.NVFP4, 9, 4016)])
 def test_batch_on_the_single_vector_path(h, fmt, N, K):
     W = synth.make_weights(fmt, N, K, seed=5 + fmt)
     Wd, _ = dev_bytes(W)
