@@ -143,6 +143,39 @@ def test_full_size_configs_on_sampled_rows(h, ci, si, fmt, N, K):
         assert np.all(np.isfinite(y))
 
 
+@pytest.mark.parametrize("fmt,N,K,mode", [(synth.Q4_K, 1_500_007, 6144, "fused"), (synth.Q4_K, 1_300_001, 6144, "split"),
+                                          (synth.NVFP4, 1_100_003, 4096, "fused"), (synth.Q8_0, 700_001, 14336, "fused")])
+def test_huge_row_counts_on_sampled_rows(h, fmt, N, K, mode):
+    """Millions of rows (5 to 11 GB of weights): the workspace limit (N * K-columns <= 4 Mi)
+    sends the long-K case with the most rows to CTAs that add their K-columns themselves, the
+    reduction-buffer budget raises the grid, and row indices pass 2^19 per launch.  The matrix
+    is a seeded block of rows tiled on the device, so row r equals base row r % n0."""
+    n0 = 4096
+    W0 = synth.make_weights(fmt, n0, K, seed=77 + fmt)
+    x = synth.make_x(fmt, K, seed=78)
+    if fmt == synth.NVFP4:  # nibble rows then scale rows: tile each part
+        nib = torch.from_numpy(W0[: n0 * (K // 2)]).cuda().view(n0, K // 2)
+        sc = torch.from_numpy(W0[n0 * (K // 2):]).cuda().view(n0, K // 16)
+        reps = (N + n0 - 1) // n0
+        Wd = torch.cat([nib.repeat(reps, 1)[:N].reshape(-1), sc.repeat(reps, 1)[:N].reshape(-1)])
+        del nib, sc
+    else:
+        rb = synth.packed_bytes(fmt, 1, K)
+        base = torch.from_numpy(W0).cuda().view(n0, rb)
+        Wd = base.repeat((N + n0 - 1) // n0, 1)[:N].reshape(-1).contiguous()
+        del base
+    assert Wd.numel() == synth.packed_bytes(fmt, N, K)
+    d = qgemv.describe(h, fmt, N, K)
+    assert f"split={int(mode == 'split')}" in d, d
+    y = run_gemv(h, fmt, dev_x(x), Wd, N, K)
+    assert qgemv.check_error(h) == qgemv.OK
+    rows = np.unique(np.concatenate([sample_rows(N, 200, seed=N), [N - 1, N - 2, min(N - 3, (1 << 20) + 5)]]))
+    y_ref, S = oracle.gemv_rows(fmt, x, W0, n0, K, rows % n0)
+    assert_parity(y.cpu().numpy()[rows], y_ref, S, f"{synth.FORMAT_NAMES[fmt]} {N}x{K} {mode}")
+    del Wd, y
+    torch.cuda.empty_cache()
+
+
 def test_config0_full(h):
     name, fmt, N, K = synth.CONFIGS[0][0]
     _check_full(h, fmt, N, K, seed=synth.config_seed(0, 0), what=name)
