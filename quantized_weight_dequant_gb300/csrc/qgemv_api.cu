@@ -38,7 +38,7 @@ struct Handle {
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
   size_t group1_smem_max[6][2][2][3] = {};  // one-format grouped kernels [format][pairs][R 2/4][D 2/3/4]
-  size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3] (Q4_K, Q5_K, Q8_0, NVFP4)
+  size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3]
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -554,7 +554,7 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
             return QGEMV_ERR_CUDA;
           }
         }
-  for (int f : {static_cast<int>(F_Q4K), static_cast<int>(F_Q5K), static_cast<int>(F_Q80), static_cast<int>(F_NVFP4)})
+  for (int f = 0; f < 6; ++f)
     for (int D : {2, 3}) {
       cudaFuncAttributes fa;
       const void* fn = batch_kernel_for(f, D);
@@ -666,11 +666,11 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   const int f = static_cast<int>(fmt);
   int64_t rb1 = 0, rb2 = 0;
   const int64_t Wk = (K / 256 + kBatchColSB - 1) / kBatchColSB;
-  // The batch kernel: two or more vectors, Q4_K / NVFP4 with streaming-eligible rows, its
+  // The batch kernel: two or more vectors, rows whose byte length is a multiple of 16, its
   // column sums in the workspace.  Otherwise each vector runs the single-vector path (which
   // is also the faster one for a single vector).
   const int warps = kBatchThreads / 32;
-  const bool fmt_ok_b = f == F_Q4K || f == F_Q5K || f == F_Q80 || f == F_NVFP4;
+  const bool fmt_ok_b = f >= 0 && f < 6;
   int D = 3;
   while (fmt_ok_b && D > 2 && batch_smem_bytes(f, warps, D) > h->batch_smem_max[f][D - 2]) --D;
   const bool batch = M > 1 && fmt_ok_b && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&

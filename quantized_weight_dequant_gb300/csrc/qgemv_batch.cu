@@ -1,4 +1,4 @@
-// Small-batch kernel instantiations (Q4_K, Q5_K, Q8_0 and NVFP4; ring depths 2 and 3).
+// Small-batch kernel instantiations (every format; ring depths 2 and 3).
 #include "qgemv_batch.cuh"
 
 namespace qg {
@@ -9,6 +9,8 @@ const void* batch_kernel_for(int f, int D) {
     case F_Q5K: return batch_kernel_table<BatchQ5K>(D);
     case F_Q80: return batch_kernel_table<BatchQ80>(D);
     case F_NVFP4: return batch_kernel_table<BatchNVFP4>(D);
+    case F_TQ10: return batch_kernel_table<BatchTQ10>(D);
+    case F_Q6K: return batch_kernel_table<BatchQ6K>(D);
   }
   return nullptr;
 }
@@ -19,6 +21,8 @@ size_t batch_smem_bytes(int f, int warps, int D) {
     case F_Q5K: return batch_smem(warps, D, batch_slice<BatchQ5K>()).total;
     case F_Q80: return batch_smem(warps, D, batch_slice<BatchQ80>()).total;
     case F_NVFP4: return batch_smem(warps, D, batch_slice<BatchNVFP4>()).total;
+    case F_TQ10: return batch_smem(warps, D, batch_slice<BatchTQ10>()).total;
+    case F_Q6K: return batch_smem(warps, D, batch_slice<BatchQ6K>()).total;
   }
   return 0;
 }

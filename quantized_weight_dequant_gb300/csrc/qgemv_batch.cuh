@@ -138,7 +138,7 @@ __device__ __forceinline__ uint32_t int2_to_h2(uint32_t lo, uint32_t hi) {
 struct BatchQ4K {
   static constexpr int kSB = 144, kSB2 = 0;
   static constexpr int kStageSB = kBatchStageSB, kPad = 16;  // superblocks per stage, slot padding
-  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false;
+  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false, kWindow = false;
 
   // x chunk of 4 fp16 values (elements e..e+3 of a superblock, e % 4 == 0) -> its slot in the
   // fragment buffer: k-step s and lane t4 part.  Byte j of chunk t4 holds element 64 t4 + j
@@ -220,7 +220,7 @@ struct BatchQ4K {
 struct BatchNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
   static constexpr int kStageSB = kBatchStageSB, kPad = 16;
-  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = true;
+  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = true, kWindow = false;
 
   // Chunk t4 of a superblock is nibble bytes [32 t4, 32 t4 + 32) = elements 64 t4 + [0, 64);
   // word i (elements 64 t4 + 8 i + [0, 8)) feeds steps 2 i (elements +0..3) and 2 i + 1
@@ -266,7 +266,7 @@ struct BatchNVFP4 {
 struct BatchQ5K {
   static constexpr int kSB = 176, kSB2 = 0;
   static constexpr int kStageSB = kBatchStageSB, kPad = 16;
-  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false;
+  static constexpr bool kMinTerm = true, kFolded = false, kBF16 = false, kWindow = false;
 
   __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
     BatchQ4K::chunk_slot(e, step, t4, v, raw);
@@ -335,7 +335,7 @@ struct BatchQ80 {
   // one superblock per stage (two would not fit 16 warps x 2 stages), slots padded by 32 so
   // the word loads of the 8 rows g fall in different banks
   static constexpr int kStageSB = 1, kPad = 32;
-  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = false;
+  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = false, kWindow = false;
 
   // elements 64 t4 + 4 s + (0..3): pairs (x0, x2) and (x1, x3), as bytes (b0, b2), (b1, b3)
   __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
@@ -380,11 +380,213 @@ struct BatchQ80 {
   }
 };
 
+// N words at a 2-byte aligned shared address: N + 1 aligned loads, each word pieced together
+// from two of them (a no-op permutation when the address is 4-byte aligned).
+template <int N>
+__device__ __forceinline__ void lds_run(uint32_t addr, uint32_t (&w)[N]) {
+  const uint32_t b = addr & ~3u, sel = 0x3210u + (addr & 2u) * 0x1111u;
+  uint32_t t[N + 1];
+#pragma unroll
+  for (int k = 0; k <= N; ++k) t[k] = lds_u32(b + 4 * k);
+#pragma unroll
+  for (int k = 0; k < N; ++k) w[k] = __byte_perm(t[k], t[k + 1], sel);
+}
+
+// ----------------------------------------------------------------------------- TQ1_0
+// Windowed formats (kWindow): their blocks (54 / 210 bytes) do not start on 16-byte
+// boundaries, so a stage copies the aligned 16-byte chunks that cover its superblocks (the
+// stage's data starts kMaxOff or fewer bytes into the slot) and reads words with lds_run.
+//
+// TQ1_0 ("ternary packing" page, the il walk): byte m of qs[0..32) holds digit n of elements
+// 32 n + m, byte 32 + m of qs holds digit n of elements 160 + 16 n + m, byte m of qh holds digit
+// n < 4 of elements 240 + 4 n + m.  Lane t4 takes qs bytes [8 t4, 8 t4 + 8) (steps 2 n + w for
+// its words w = 0, 1), qs bytes [32 + 4 t4, 36 + 4 t4) (steps 10 + n) and digit n = t4 of the
+// qh word (step 15).  The digits come out of the floor pair as in the stream decoder: with the
+// even and the odd bytes in 16-bit lanes, q <- 3 q splits into the digit (bits 8..9) and the
+// rest (bits 0..7); the digit, put into the fp16 mantissa of 1024, is scaled to t - 1 with one
+// exact half FMA: (1024 + 256 t) / 256 - 5.  A superblock's sums get its d in fp32.
+struct BatchTQ10 {
+  static constexpr int kSB = 54, kSB2 = 0;
+  static constexpr int kStageSB = 4, kPad = 16, kMaxOff = 8;  // stage starts at 216 wk: offset 0 or 8
+  static constexpr bool kMinTerm = false, kFolded = false, kBF16 = false, kWindow = true;
+
+  __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
+    if (e < 160) {
+      const int m = e & 31;
+      t4 = m >> 3;
+      step = 2 * (e >> 5) + ((m >> 2) & 1);
+    } else if (e < 240) {
+      t4 = ((e - 160) & 15) >> 2;
+      step = 10 + ((e - 160) >> 4);
+    } else {
+      t4 = (e - 240) >> 2;
+      step = 15;
+    }
+    v.x = __byte_perm(raw.x, raw.y, 0x5410);  // (x0, x2)
+    v.y = __byte_perm(raw.x, raw.y, 0x7632);  // (x1, x3)
+  }
+
+  // The lane's words of one row: qs region 1 (2 words), region 2 (1 word), qh and d.
+  __device__ __forceinline__ static void row_words(uint32_t blk, int t4, uint32_t (&w1)[2], uint32_t& w2, uint32_t& wh,
+                                                   float& d) {
+    lds_run<2>(blk + 8 * t4, w1);
+    uint32_t r2[1], th[2];
+    lds_run<1>(blk + 32 + 4 * t4, r2);
+    lds_run<2>(blk + 48, th);
+    w2 = r2[0];
+    wh = th[0];
+    d = h2f(th[1]);
+  }
+
+  // Next digit of the (even or odd byte) lanes q: returns t - 1 as an fp16 pair.
+  __device__ __forceinline__ static uint32_t digit(uint32_t& q, uint32_t magic) {
+    const uint32_t r = q * 3u;
+    q = r & 0x00FF00FFu;
+    return hfma2_u(and_or<0x03000300u>(r, magic), 0x1C001C00u, 0xC500C500u);  // x 2^-8, - 5
+  }
+
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t,
+                                                    uint32_t magic, float (&y)[4]) {
+    uint32_t ag[2], a8[2], bg, b8, hg, h8;
+    float dg, d8;
+    row_words(rg + kSB * c, t4, ag, bg, hg, dg);
+    row_words(r8 + kSB * c, t4, a8, b8, h8, d8);
+    float dq[2][4] = {};
+    auto steps = [&](uint32_t wg, uint32_t w8, int s0, int ds) {
+      uint32_t eg = wg & 0x00FF00FFu, og = (wg >> 8) & 0x00FF00FFu;
+      uint32_t e8 = w8 & 0x00FF00FFu, o8 = (w8 >> 8) & 0x00FF00FFu;
+#pragma unroll
+      for (int n = 0; n < 5; ++n) {
+        const int s = s0 + ds * n;
+        const uint2 xv = lds_v2(xa + s * 256);
+        const uint32_t A0 = digit(eg, magic), A1 = digit(e8, magic), A2 = digit(og, magic), A3 = digit(o8, magic);
+        mma16816(dq[n & 1], A0, A1, A2, A3, xv.x, xv.y);
+      }
+    };
+    steps(ag[0], a8[0], 0, 2);
+    steps(ag[1], a8[1], 1, 2);
+    steps(bg, b8, 10, 1);
+    {  // qh: digit t4 of each byte, q = b 3^t4 mod 256 first
+      const uint32_t p3 = (t4 & 2 ? 9u : 1u) * (t4 & 1 ? 3u : 1u);
+      uint32_t eg = ((hg & 0x00FF00FFu) * p3) & 0x00FF00FFu, og = (((hg >> 8) & 0x00FF00FFu) * p3) & 0x00FF00FFu;
+      uint32_t e8 = ((h8 & 0x00FF00FFu) * p3) & 0x00FF00FFu, o8 = (((h8 >> 8) & 0x00FF00FFu) * p3) & 0x00FF00FFu;
+      const uint2 xv = lds_v2(xa + 15 * 256);
+      const uint32_t A0 = digit(eg, magic), A1 = digit(e8, magic), A2 = digit(og, magic), A3 = digit(o8, magic);
+      mma16816(dq[1], A0, A1, A2, A3, xv.x, xv.y);
+    }
+    y[0] += dg * (dq[0][0] + dq[1][0]);
+    y[1] += dg * (dq[0][1] + dq[1][1]);
+    y[2] += d8 * (dq[0][2] + dq[1][2]);
+    y[3] += d8 * (dq[0][3] + dq[1][3]);
+  }
+};
+
+// ----------------------------------------------------------------------------- Q6_K
+// Element i = 128 H + 32 r + l (half H, quarter r, l < 32): low four bits in ql[64 H + 32 (r & 1)
+// + l] (low nibble for r < 2), top two bits (qh[32 H + l] >> 2 r) & 3, scale sc[8 H + 2 r +
+// l / 16].  Lane t4 takes l in [8 t4, 8 t4 + 8): step 8 H + 2 r + u reads word u of that range,
+// whose four elements share the scale sc[8 H + 2 r + t4 / 2].  A = (q6 - 32) sc in fp16: exact
+// while |(q6 - 32) sc| <= 2048 (scales up to 64 in magnitude), else rounded once, a relative
+// error of at most 2^-11 per weight.  One superblock per stage (two would not fit).
+struct BatchQ6K {
+  static constexpr int kSB = 210, kSB2 = 0;
+  static constexpr int kStageSB = 1, kPad = 16, kMaxOff = 14;  // superblock j starts at 2 j mod 16
+  static constexpr bool kMinTerm = false, kFolded = false, kBF16 = false, kWindow = true;
+
+  __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
+    const int l = e & 31;
+    t4 = l >> 3;
+    step = 8 * (e >> 7) + 2 * ((e >> 5) & 3) + ((l >> 2) & 1);
+    v.x = __byte_perm(raw.x, raw.y, 0x5410);
+    v.y = __byte_perm(raw.x, raw.y, 0x7632);
+  }
+
+  struct Row {
+    uint32_t ql[2][2][2];  // [H][r & 1][u]
+    uint32_t qh[2][2];     // [H][u]
+    uint32_t sc[4];        // sc[0..16)
+    float d;
+  };
+  __device__ __forceinline__ static void row_words(uint32_t blk, int t4, Row& R) {
+#pragma unroll
+    for (int H = 0; H < 2; ++H) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) lds_run<2>(blk + 64 * H + 32 * j + 8 * t4, R.ql[H][j]);
+      lds_run<2>(blk + 128 + 32 * H + 8 * t4, R.qh[H]);
+    }
+    uint32_t t[5];
+    lds_run<5>(blk + 192, t);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) R.sc[k] = t[k];
+    R.d = h2f(t[4]);
+  }
+
+  // fp16 pair (s, s) of int8 byte k of word w (k a run-time index 0..3)
+  __device__ __forceinline__ static uint32_t scale2(uint32_t w, uint32_t sel) {
+    return hsub2_u((__byte_perm(w, 0u, sel) ^ 0x00800080u) | 0x64006400u, 0x64806480u);  // (1152 + s) - 1152
+  }
+
+  // fp16 (1024 + q6) pairs of the even (e) and odd (o) bytes of word u, quarter r
+  template <int R>
+  __device__ __forceinline__ static void codes(uint32_t ql, uint32_t qh, uint32_t magic, uint32_t& e, uint32_t& o) {
+    constexpr int sl = 4 * (R >> 1);
+    const uint32_t he = R < 3 ? (qh << (4 - 2 * R)) : (qh >> 2);  // bits 2R..2R+1 of bytes 0, 2 to 4..5
+    const uint32_t ho = qh >> (4 + 2 * R);                          // of bytes 1, 3
+    e = and_or<0x000F000Fu>(ql >> sl, and_or<0x00300030u>(he, magic));
+    o = and_or<0x000F000Fu>(ql >> (8 + sl), and_or<0x00300030u>(ho, magic));
+  }
+
+  __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t,
+                                                    uint32_t magic, float (&y)[4]) {
+    Row G, E;
+    row_words(rg + kSB * c, t4, G);
+    row_words(r8 + kSB * c, t4, E);
+    const uint32_t hb = static_cast<uint32_t>(t4 >> 1);
+    const uint32_t sel0 = 0x4040u | hb | (hb << 8), sel1 = sel0 + 0x0202u;  // bytes hb / hb + 2, in both lanes
+    const uint32_t off = 0x64206420u;  // fp16 (1056, 1056) = 1024 + 32
+    float dq[2][4] = {};
+#pragma unroll
+    for (int H = 0; H < 2; ++H) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t sw = (r & 1) ? sel1 : sel0;
+        const uint32_t sg = scale2(G.sc[2 * H + (r >> 1)], sw), s8 = scale2(E.sc[2 * H + (r >> 1)], sw);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint32_t eg, og, e8, o8;
+          switch (r) {
+            case 0: codes<0>(G.ql[H][0][u], G.qh[H][u], magic, eg, og), codes<0>(E.ql[H][0][u], E.qh[H][u], magic, e8, o8); break;
+            case 1: codes<1>(G.ql[H][1][u], G.qh[H][u], magic, eg, og), codes<1>(E.ql[H][1][u], E.qh[H][u], magic, e8, o8); break;
+            case 2: codes<2>(G.ql[H][0][u], G.qh[H][u], magic, eg, og), codes<2>(E.ql[H][0][u], E.qh[H][u], magic, e8, o8); break;
+            default: codes<3>(G.ql[H][1][u], G.qh[H][u], magic, eg, og), codes<3>(E.ql[H][1][u], E.qh[H][u], magic, e8, o8); break;
+          }
+          const int s = 8 * H + 2 * r + u;
+          const uint2 xv = lds_v2(xa + s * 256);
+          mma16816(dq[u], hmul2_u(hsub2_u(eg, off), sg), hmul2_u(hsub2_u(e8, off), s8), hmul2_u(hsub2_u(og, off), sg),
+                   hmul2_u(hsub2_u(o8, off), s8), xv.x, xv.y);
+        }
+      }
+    }
+    y[0] += G.d * (dq[0][0] + dq[1][0]);
+    y[1] += G.d * (dq[0][1] + dq[1][1]);
+    y[2] += E.d * (dq[0][2] + dq[1][2]);
+    y[3] += E.d * (dq[0][3] + dq[1][3]);
+  }
+};
+
 // Bytes of one row slot in a ring stage: the row's superblocks of the stage (stream 1, then
-// stream 2) plus padding, so that the 16 rows of a stage start in different shared-memory banks.
+// stream 2; for windowed formats the covering aligned chunks) plus padding, so that the 16
+// rows of a stage start in different shared-memory banks.
+template <class Fmt>
+__host__ __device__ constexpr int batch_chunks() {
+  if constexpr (Fmt::kWindow)
+    return (Fmt::kMaxOff + Fmt::kStageSB * Fmt::kSB + 15) / 16;
+  else
+    return Fmt::kStageSB * (Fmt::kSB + Fmt::kSB2) / 16;
+}
 template <class Fmt>
 __host__ __device__ constexpr int batch_slice() {
-  return Fmt::kStageSB * (Fmt::kSB + Fmt::kSB2) + Fmt::kPad;
+  return 16 * batch_chunks<Fmt>() + Fmt::kPad;
 }
 
 template <class Fmt, int D>
@@ -414,10 +616,11 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
   // stream 2); lane l copies chunks l + 32 j, whose row, source offset (from the stage's row
   // block) and slot offset are fixed per lane.
   constexpr int SSB = Fmt::kStageSB;
-  constexpr int CPR = SSB * (SB + SB2) / 16;
+  constexpr int CPR = batch_chunks<Fmt>();
   constexpr int NCH = kBatchRows * CPR;  // chunks per stage
   constexpr int JN = (NCH + 31) / 32;
   const int rb1 = static_cast<int>(a.row_bytes), rb2 = static_cast<int>(a.row_bytes2);
+  // csb: windowed formats: the chunk's first byte in the window; otherwise its superblock
   uint32_t coff[JN], doff[JN], crow[JN], csb[JN], c2[JN];
 #pragma unroll
   for (int j = 0; j < JN; ++j) {
@@ -425,7 +628,10 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     const bool two = kTwo && off >= SSB * SB / 16;
     const int o2 = off - SSB * SB / 16;
     coff[j] = two ? row * rb2 + o2 * 16 : row * rb1 + off * 16;
-    csb[j] = q < NCH ? (two ? o2 : (off * 16) / SB) : SSB;  // chunks past the stage: never copied
+    if constexpr (Fmt::kWindow)
+      csb[j] = q < NCH ? off * 16 : 0x7fffffff;  // chunks past the stage: never copied
+    else
+      csb[j] = q < NCH ? (two ? o2 : (off * 16) / SB) : SSB;
     crow[j] = row;
     c2[j] = two;
     doff[j] = row * SLICE + off * 16;
@@ -439,13 +645,25 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
       const int trows = min(kBatchRows, nrows - tile * kBatchRows);
       const int64_t r0 = p_lo + tile * kBatchRows;
       const int sb0 = kBatchColSB * wk + SSB * h;  // first superblock of the stage in the row
-      const uint8_t* base1 = a.W + r0 * a.row_bytes + static_cast<int64_t>(sb0) * SB;
-      const uint8_t* base2 = kTwo ? a.W2 + r0 * a.row_bytes2 + static_cast<int64_t>(sb0) * SB2 : base1;
       const int nsb_left = ncols - SSB * h;
+      if constexpr (Fmt::kWindow) {
+        // the stage's bytes start o bytes into their 16-byte chunk (rows are 16-byte multiples)
+        const int o = (sb0 * SB) & 15;
+        const uint8_t* base1 = a.W + r0 * a.row_bytes + static_cast<int64_t>(sb0) * SB - o;
+        const int need = o + min(SSB, nsb_left) * SB;
 #pragma unroll
-      for (int j = 0; j < JN; ++j) {
-        const uint32_t ok = (static_cast<int>(crow[j]) < trows) & (static_cast<int>(csb[j]) < nsb_left);
-        cp_async16_if<0, 0>(slot_sa + doff[j], (c2[j] ? base2 : base1) + coff[j], ok);
+        for (int j = 0; j < JN; ++j) {
+          const uint32_t ok = (static_cast<int>(crow[j]) < trows) & (static_cast<int>(csb[j]) < need);
+          cp_async16_if<0, 0>(slot_sa + doff[j], base1 + coff[j], ok);
+        }
+      } else {
+        const uint8_t* base1 = a.W + r0 * a.row_bytes + static_cast<int64_t>(sb0) * SB;
+        const uint8_t* base2 = kTwo ? a.W2 + r0 * a.row_bytes2 + static_cast<int64_t>(sb0) * SB2 : base1;
+#pragma unroll
+        for (int j = 0; j < JN; ++j) {
+          const uint32_t ok = (static_cast<int>(crow[j]) < trows) & (static_cast<int>(csb[j]) < nsb_left);
+          cp_async16_if<0, 0>(slot_sa + doff[j], (c2[j] ? base2 : base1) + coff[j], ok);
+        }
       }
     }
     cp_async_commit();
@@ -550,7 +768,12 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_kernel(const __grid_co
     cp_async_wait<D - 1>();
     __syncwarp();
     const int tile = st / spt, h = st - tile * spt;
-    const uint32_t rg = cs + g * SLICE, r8 = cs + (g + 8) * SLICE;
+    uint32_t rg = cs + g * SLICE, r8 = cs + (g + 8) * SLICE;
+    if constexpr (Fmt::kWindow) {
+      const uint32_t o = static_cast<uint32_t>((kBatchColSB * wk + SSB * h) * SB) & 15u;
+      rg += o;
+      r8 += o;
+    }
 #pragma unroll
     for (int c = 0; c < SSB; ++c) {
       const int sbk = SSB * h + c;  // superblock within the K-column

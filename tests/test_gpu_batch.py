@@ -1,8 +1,9 @@
 """GPU parity of the small-batch GEMV (qgemv_run_batch): M = 1..8 activation vectors against
 the oracle, one vector at a time, each output within |y - y_ref| <= 2e-3 * sum|x w| + 1e-5
-of its own vector.  Q4_K, Q5_K, Q8_0 and NVFP4 run the mma.sync kernel (one to fourteen
-K-columns, ragged row counts, partial last K-columns) for M >= 2; M = 1, Q6_K, TQ1_0 and
-shapes the streaming kernels do not take run the single-vector path per vector."""
+of its own vector.  Every format runs the mma.sync kernel for M >= 2 (one to fourteen
+K-columns, ragged row counts, partial last K-columns; TQ1_0 and Q6_K, whose blocks are not
+16-byte aligned, through copy windows at every window offset); M = 1 and rows whose byte
+length is not a multiple of 16 run the single-vector path per vector."""
 import numpy as np
 import pytest
 import torch
@@ -57,7 +58,9 @@ def _run(h, fmt, X, W_dev, N, K):
 SHAPES = [(synth.Q4_K, 77, 2048), (synth.Q4_K, 300, 4096), (synth.Q4_K, 129, 14336), (synth.Q4_K, 8, 2304),
           (synth.Q4_K, 1, 256), (synth.NVFP4, 65, 2048), (synth.NVFP4, 40, 14336), (synth.NVFP4, 333, 4352),
           (synth.NVFP4, 3, 256), (synth.Q5_K, 77, 4096), (synth.Q5_K, 33, 12288), (synth.Q5_K, 5, 768),
-          (synth.Q8_0, 65, 4096), (synth.Q8_0, 40, 12288), (synth.Q8_0, 17, 1280)]
+          (synth.Q8_0, 65, 4096), (synth.Q8_0, 40, 12288), (synth.Q8_0, 17, 1280),
+          (synth.TQ1_0, 77, 4096), (synth.TQ1_0, 300, 2048), (synth.TQ1_0, 33, 14336), (synth.TQ1_0, 9, 6144),
+          (synth.Q6_K, 65, 4096), (synth.Q6_K, 40, 12288), (synth.Q6_K, 129, 2048), (synth.Q6_K, 7, 6144)]
 
 
 @pytest.mark.parametrize("fmt,N,K", SHAPES)
@@ -71,8 +74,8 @@ def test_batch_matches_oracle(h, fmt, N, K, M):
     assert qgemv.check_error(h) == qgemv.OK
 
 
-@pytest.mark.parametrize("fmt,N,K", [(synth.Q6_K, 40, 12288), (synth.TQ1_0, 33, 4096), (synth.Q8_0, 50, 4000),
-                                     (synth.Q6_K, 17, 2048), (synth.NVFP4, 9, 4016)])
+@pytest.mark.parametrize("fmt,N,K", [(synth.Q6_K, 40, 2816), (synth.TQ1_0, 33, 2304), (synth.Q8_0, 50, 4000),
+                                     (synth.Q6_K, 17, 1024), (synth.TQ1_0, 20, 4352), (synth.NVFP4, 9, 4016)])
 def test_batch_on_the_single_vector_path(h, fmt, N, K):
     W = synth.make_weights(fmt, N, K, seed=5 + fmt)
     Wd, _ = dev_bytes(W)
@@ -81,7 +84,7 @@ def test_batch_on_the_single_vector_path(h, fmt, N, K):
     _check(Y, X, fmt, W, N, K, what=f"{synth.FORMAT_NAMES[fmt]} {N}x{K}")
 
 
-@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.NVFP4])
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.NVFP4, synth.TQ1_0, synth.Q6_K])
 def test_batch_vectors_are_independent_and_deterministic(h, fmt):
     """Vector m of a batch equals the single-vector batch of the same x (the other vectors do
     not leak into it), within the GEMV bound, and repeated calls are bit-identical."""
@@ -127,7 +130,8 @@ def test_batch_rejects_bad_arguments(h):
 
 
 @pytest.mark.parametrize("fmt,N,K,M", [(synth.Q4_K, 4096, 14336, 8), (synth.Q4_K, 28672, 4096, 4),
-                                       (synth.NVFP4, 4096, 14336, 8), (synth.NVFP4, 14336, 4096, 2)])
+                                       (synth.NVFP4, 4096, 14336, 8), (synth.NVFP4, 14336, 4096, 2),
+                                       (synth.TQ1_0, 11008, 4096, 8), (synth.Q6_K, 4096, 12288, 8)])
 def test_batch_full_size_sampled_rows(h, fmt, N, K, M):
     W = synth.make_weights(fmt, N, K, seed=21 + fmt)
     Wd, _ = dev_bytes(W)
