@@ -129,8 +129,9 @@ int qgemv_group_size(qgemv_format_t fmt);
 /* Tuning and test options (per handle).  Values are validated; bad ones give
  * QGEMV_ERR_INVALID_ARG and change nothing.
  *   QGEMV_OPT_FORCE_PATH      0 auto, 1 the cp.async streaming kernels (falls back to 0
- *                             when the shape does not meet their alignment rule), 2 the
- *                             plain warp-per-row kernels.
+ *                             when the shape does not meet their alignment rule) and, in
+ *                             qgemv_run_batch, the batch kernel for every M >= 2 it takes
+ *                             (whatever N), 2 the plain warp-per-row kernels.
  *   QGEMV_OPT_RING_DEPTH      0 auto, else 2..8: copy stages per warp of the streaming
  *                             kernel (2, 3 or 4 are used, larger values mean 4; fewer
  *                             if they do not fit in shared memory).
@@ -248,11 +249,13 @@ qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x,
 /* ---------------------------------------------------------------- small batches
  * Y = X . dequant(W)^T for M = 1..QGEMV_MAX_BATCH activation vectors at once (the general
  * GEMV of the Q4_K page, "What is a GEMV", with x of shape (M, K) instead of (1, K)): every
- * packed weight is read and decoded once and serves all M vectors.  For M >= 2, Q4_K, Q5_K,
- * Q8_0 and NVFP4 with K a multiple of 256 use the tensor cores' mma.sync path (decoded weights
- * go straight into the A fragments; the M vectors fill the B operand), as long as
- * M * N * ceil(K / 1024) fits the handle's workspace (4 Mi column sums); M = 1, Q6_K, TQ1_0
- * and other shapes run the single-vector path once per vector. */
+ * packed weight is read and decoded once and serves all M vectors.  Every format uses the
+ * tensor cores' mma.sync path (decoded weights go straight into the A fragments; the M vectors
+ * fill the B operand) when M >= 4, or M >= 2 and N >= 4096 (below that two or three
+ * single-vector launches are faster), with rows whose packed length is a multiple of 16 bytes
+ * (K a multiple of 2048 for TQ1_0 and Q6_K, of 256 for the others) and M * N * ceil(K / 1024)
+ * within the handle's workspace (4 Mi column sums); other calls run the single-vector path
+ * once per vector. */
 #define QGEMV_MAX_BATCH 8
 
 /* x: device, M rows of K 16-bit values (fp16; bf16 for NVFP4), row-major, 16-byte aligned.

@@ -673,7 +673,10 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   const bool fmt_ok_b = f >= 0 && f < 6;
   int D = 3;
   while (fmt_ok_b && D > 2 && batch_smem_bytes(f, warps, D) > h->batch_smem_max[f][D - 2]) --D;
-  const bool batch = M > 1 && fmt_ok_b && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
+  // Below 4096 rows a warp's 16-row tiles hold a row or two, and the kernel's latency (a few
+  // dependent copy rounds plus the column reduction) exceeds two or three short launches.
+  const bool worth = M >= 4 || N >= 4096 || h->force_path == 1;
+  const bool batch = M > 1 && worth && fmt_ok_b && h->force_path != 2 && stream_rows(f, K, rb1, rb2) &&
                      batch_smem_bytes(f, warps, D) <= h->batch_smem_max[f][D - 2] &&
                      (Wk == 1 || static_cast<double>(M) * N * Wk <= static_cast<double>(kWsFloats));
   if (!batch) {

@@ -47,11 +47,17 @@ def _check(Y, X, fmt, W, N, K, rows=None, what=""):
         assert bad.size == 0, f"{what} vector {m}: {bad.size} outside, first {bad[:5]} err {err[bad[:5]]}"
 
 
-def _run(h, fmt, X, W_dev, N, K):
+def _run(h, fmt, X, W_dev, N, K, force=1):
+    """force=1: the batch kernel for every M >= 2 (the automatic choice sends two or three
+    vectors of fewer than 4096 rows to the single-vector path)."""
     M = X.shape[0]
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    qgemv.run_batch(h, fmt, _dev_x(X), M, W_dev, N, K, y)
-    torch.cuda.synchronize()
+    qgemv.set_option(h, qgemv.OPT_FORCE_PATH, force)
+    try:
+        qgemv.run_batch(h, fmt, _dev_x(X), M, W_dev, N, K, y)
+        torch.cuda.synchronize()
+    finally:
+        qgemv.set_option(h, qgemv.OPT_FORCE_PATH, 0)
     return y.cpu().numpy()
 
 
@@ -101,6 +107,18 @@ def test_batch_vectors_are_independent_and_deterministic(h, fmt):
         Ys = _run(h, fmt, X[m:m + 1], Wd, N, K)
         _, S = oracle.gemv(fmt, X[m], W, N, K)
         assert np.all(np.abs(Ys[0].astype(np.float64) - Y1[m]) <= 2 * (RTOL * S + ATOL))
+
+
+@pytest.mark.parametrize("fmt,N,M", [(synth.Q6_K, 1024, 2), (synth.Q5_K, 1024, 3), (synth.Q4_K, 4096, 2),
+                                     (synth.Q6_K, 1024, 4)])
+def test_batch_automatic_path_choice(h, fmt, N, M):
+    """The automatic choice (both ways of it) meets the same bound."""
+    K = 4096
+    W = synth.make_weights(fmt, N, K, seed=6 + fmt)
+    Wd, _ = dev_bytes(W)
+    X = _xs(fmt, M, K, seed=12)
+    Y = _run(h, fmt, X, Wd, N, K, force=0)
+    _check(Y, X, fmt, W, N, K, what=f"auto {synth.FORMAT_NAMES[fmt]} {N}x{K} M={M}")
 
 
 def test_batch_nvfp4_wide_range_vectors(h):
