@@ -267,6 +267,28 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t h, qgemv_format_t fmt, const void*
                                const void* packed_W, int64_t N, int64_t K, float* y,
                                cudaStream_t stream);
 
+/* ---------------------------------------------------------------- many rows (prefill)
+ * Y = X . dequant(W)^T for any number M >= 1 of activation rows: the matrix-matrix product
+ * that the Mojo "fp4_gemv" page sets beside its GEMV (its opening description: a whole prompt
+ * goes through the prefill path, a shared-memory tile feeding the matrix unit, while decode
+ * at M = 1 is the GEMV).  NVFP4 with M > QGEMV_MAX_BATCH and K a multiple of 64 runs on the
+ * fifth-generation tensor cores (tcgen05): tiles of 128 weight rows x 256 (M <= 128: 128)
+ * rows of X, X brought in by TMA, the weights dequantised exactly to bf16 into the
+ * shared-memory operand tile (e2m1 times an e4m3 scale has at most 6 significant bits), fp32
+ * accumulation in tensor memory.  Every other call goes through qgemv_run_batch in chunks of
+ * QGEMV_MAX_BATCH rows.
+ *
+ * x: device, M rows of K 16-bit values (fp16; bf16 for NVFP4), row-major, 16-byte aligned.
+ * y: device, M rows of N fp32 values, row-major (y[m * N + n]), 16-byte aligned.
+ * packed_W, N, K: as qgemv_run.  M < 1 gives QGEMV_ERR_INVALID_ARG; the tensor-core path
+ * needs M, K < 2^31 (else QGEMV_ERR_BAD_SHAPE).  Asynchronous on `stream`, allocates
+ * nothing; each output obeys the GEMV tolerance of its own row; repeated calls give identical
+ * bits.  A wait in the tensor-core kernel that runs past QGEMV_OPT_SPIN_LIMIT_NS sets the
+ * handle's error word (read by qgemv_check_error). */
+qgemv_status_t qgemv_run_gemm(qgemv_handle_t h, qgemv_format_t fmt, const void* x, int64_t M,
+                              const void* packed_W, int64_t N, int64_t K, float* y,
+                              cudaStream_t stream);
+
 /* Capacity of qgemv_run_noalloc's scratch, in fp32 column sums: N * ceil(K / 2048) of them. */
 #define QGEMV_NOALLOC_MAX_COLUMN_SUMS 262144
 

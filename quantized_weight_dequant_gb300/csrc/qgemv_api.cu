@@ -1,4 +1,5 @@
 // C-ABI of libqgemv: validation, launch planning and launches.  See include/qgemv.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -7,6 +8,7 @@
 #include <new>
 
 #include "../../include/qgemv.h"
+#include "qgemm_tc.cuh"
 #include "qgemv_batch.cuh"
 #include "qgemv_simple.cuh"
 #include "qgemv_stream.cuh"
@@ -39,6 +41,8 @@ struct Handle {
   size_t group_smem_max[2][3] = {};   // mixed-format grouped kernel [R 2/4][D 2/3/4]
   size_t group1_smem_max[6][2][2][3] = {};  // one-format grouped kernels [format][pairs][R 2/4][D 2/3/4]
   size_t batch_smem_max[6][2] = {};          // small-batch kernels [format][D 2/3]
+  void* encode_tiled = nullptr;              // the driver's cuTensorMapEncodeTiled (null: no TMA path)
+  int tc_cluster_max[3] = {1, 1, 1};         // largest cluster (K splits) the GEMM kernels can run [BT 64/128/256]
   int force_path = 0;
   int ring_depth = 0;
   int rows_per_stage = 0;
@@ -143,6 +147,7 @@ const void* group_kernel_pair_tq10(int R, int D);
 const void* group_kernel_pair_nvfp4(int R, int D);
 const void* batch_kernel_for(int f, int D);
 size_t batch_smem_bytes(int f, int warps, int D);
+const void* tc_kernel_for(int BT);
 }  // namespace qg
 
 namespace {
@@ -569,6 +574,42 @@ qgemv_status_t qgemv_create(qgemv_handle_t* out, int device) {
         return QGEMV_ERR_CUDA;
       }
     }
+  // The tensor-core GEMM needs TMA descriptors, encoded by the driver; without the entry point
+  // qgemv_run_gemm keeps to the batch path.
+  {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      h->encode_tiled = fn;
+    cudaGetLastError();
+  }
+  for (int BT : {64, 128, 256}) {
+    if (cudaFuncSetAttribute(tc_kernel_for(BT), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tc_smem_bytes(BT))) != cudaSuccess) {
+      release();
+      return QGEMV_ERR_CUDA;
+    }
+    for (int cs : {8, 4, 2}) {  // the largest cluster of these CTAs that the GPU can place
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+      cfg.blockDim = dim3(kTcThreads, 1, 1);
+      cfg.dynamicSmemBytes = tc_smem_bytes(BT);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = static_cast<unsigned>(cs);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, tc_kernel_for(BT), &cfg) == cudaSuccess && nc >= 1) {
+        h->tc_cluster_max[BT > 128 ? 2 : BT > 64 ? 1 : 0] = cs;
+        break;
+      }
+      cudaGetLastError();
+    }
+  }
   *out = reinterpret_cast<qgemv_handle_t>(h);
   return QGEMV_OK;
 }
@@ -721,6 +762,82 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t hh, qgemv_format_t fmt, const void
   }
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, batch_kernel_for(f, D), args) != cudaSuccess) {
+    cudaGetLastError();
+    return QGEMV_ERR_CUDA;
+  }
+  return QGEMV_OK;
+}
+
+qgemv_status_t qgemv_run_gemm(qgemv_handle_t hh, qgemv_format_t fmt, const void* x, int64_t M, const void* W, int64_t N,
+                              int64_t K, float* y, cudaStream_t stream) {
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  qgemv_status_t st = validate(h, fmt, W, N, K);
+  if (st != QGEMV_OK) return st;
+  if (!x || !y || M < 1) return QGEMV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return QGEMV_ERR_MISALIGNED;
+  const int f = static_cast<int>(fmt);
+  const bool tc = f == F_NVFP4 && M > QGEMV_MAX_BATCH && K % kTcBK == 0 && h->encode_tiled && h->force_path != 2 &&
+                  tc_smem_bytes(256) <= h->smem_optin;
+  if (!tc) {
+    for (int64_t m0 = 0; m0 < M; m0 += QGEMV_MAX_BATCH) {
+      const int mb = static_cast<int>(std::min<int64_t>(QGEMV_MAX_BATCH, M - m0));
+      st = qgemv_run_batch(hh, fmt, static_cast<const uint16_t*>(x) + m0 * K, mb, W, N, K, y + m0 * N, stream);
+      if (st != QGEMV_OK) return st;
+    }
+    return QGEMV_OK;
+  }
+  if (M > 0x7fffffff || K > 0x7fffffff) return QGEMV_ERR_BAD_SHAPE;
+  const int BT = M > 128 ? 256 : M > 64 ? 128 : 64;
+  const int64_t ntt = (M + BT - 1) / BT, nwt = (N + kTcRows - 1) / kTcRows;
+  if (ntt * nwt > 0x7fffffff) return QGEMV_ERR_BAD_SHAPE;
+  // X as a 2-D tensor (K innermost, M rows), read in boxes of 64 x BT with the 128-byte swizzle
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(BT)};
+  const cuuint32_t estr[2] = {1, 1};
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                                const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  if (reinterpret_cast<EncodeFn>(h->encode_tiled)(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
+                                                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QGEMV_ERR_CUDA;
+  // Split K over the CTAs of a cluster when the tiles fill fewer than all SMs: as many splits
+  // as whole waves of tiles fit, at least four K-blocks each, at most the largest cluster.
+  const int64_t tiles = ntt * nwt, nk = K / kTcBK;
+  int64_t ks = 1;
+  if (tiles < h->sms)
+    ks = std::min<int64_t>({h->sms / tiles, std::max<int64_t>(1, nk / 4), h->tc_cluster_max[BT > 128 ? 2 : BT > 64 ? 1 : 0]});
+  int64_t kb_per = (nk + ks - 1) / ks;
+  while (ks > 1 && (ks - 1) * kb_per >= nk) --ks;  // every split gets at least one K-block
+  TcArgs a{};
+  a.W = static_cast<const uint8_t*>(W);
+  a.S = a.W + N * (K / 2);
+  a.y = y;
+  a.N = N;
+  a.T = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.n_ttiles = static_cast<int>(ntt);
+  a.ks = static_cast<int>(ks);
+  a.kb_per = static_cast<int>(kb_per);
+  a.err = h->err;
+  a.spin_ns = h->spin_ns;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * ks), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc_smem_bytes(BT);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&map, &a};
+  if (cudaLaunchKernelExC(&cfg, tc_kernel_for(BT), args) != cudaSuccess) {
     cudaGetLastError();
     return QGEMV_ERR_CUDA;
   }

@@ -33,7 +33,8 @@ class Problem(ctypes.Structure):
 
 EXPORTS = ["qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
            "qgemv_status_string", "qgemv_packed_bytes", "qgemv_group_size", "qgemv_set_option",
-           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc", "qgemv_run_group", "qgemv_run_ex", "qgemv_run_batch"]
+           "qgemv_describe", "qgemv_build_marker", "qgemv_run_noalloc", "qgemv_run_group", "qgemv_run_ex", "qgemv_run_batch",
+           "qgemv_run_gemm"]
 
 _lib = None
 
@@ -70,9 +71,10 @@ def lib() -> ctypes.CDLL:
         L.qgemv_run_ex.argtypes = [vp, ctypes.c_int, vp, vp, i64, i64, ctypes.c_float, ctypes.c_float, vp,
                                    ctypes.c_int, vp]
         L.qgemv_run_batch.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, i64, i64, vp, vp]
+        L.qgemv_run_gemm.argtypes = [vp, ctypes.c_int, vp, i64, vp, i64, i64, vp, vp]
         for name in ("qgemv_create", "qgemv_destroy", "qgemv_run", "qgemv_unpack", "qgemv_check_error",
                      "qgemv_set_option", "qgemv_describe", "qgemv_run_noalloc", "qgemv_run_group",
-                     "qgemv_run_ex", "qgemv_run_batch"):
+                     "qgemv_run_ex", "qgemv_run_batch", "qgemv_run_gemm"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -181,6 +183,15 @@ def run_batch(h: Handle, fmt: int, x, M: int, packed_W, N: int, K: int, y, strea
     st = lib().qgemv_run_batch(h.ptr, fmt, _ptr(x), M, _ptr(packed_W), N, K, _ptr(y), _stream(stream))
     if check:
         _check(st, "qgemv_run_batch")
+    return st
+
+
+def run_gemm(h: Handle, fmt: int, x, M: int, packed_W, N: int, K: int, y, stream=None, check: bool = True) -> int:
+    """Y = X . dequant(W)^T for any number M of row-major activation rows x [M, K] (NVFP4 with
+    M > MAX_BATCH on the tcgen05 tensor-core kernel)."""
+    st = lib().qgemv_run_gemm(h.ptr, fmt, _ptr(x), M, _ptr(packed_W), N, K, _ptr(y), _stream(stream))
+    if check:
+        _check(st, "qgemv_run_gemm")
     return st
 
 
