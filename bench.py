@@ -304,6 +304,113 @@ def run_profile_launches(args, gemvs):
     return 0
 
 
+def load_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def run_prefill(args, gemvs, rank, world):
+    """`--prefill M`: the NVFP4 GEMM of M activation rows (qgemv_run_gemm, the tcgen05
+    tensor-core kernel for M > 8) on the workload's NVFP4 matrices, timed with CUDA events
+    over --steps launches after --warmup, weight copies rotated so that W and X together
+    exceed L2 three times.  One JSON line: TFLOP/s against the dense bf16 tensor peak."""
+    import torch
+
+    from quantized_weight_dequant_gb300 import qgemv
+    from quantized_weight_dequant_gb300.build import build_library
+
+    shapes = [(lab, n, k) for lab, f, n, k, _ in gemvs if f == synth.NVFP4]
+    if not shapes:
+        raise SystemExit(f"--prefill: workload {args.workload} has no NVFP4 matrix")
+    if world > 1 and rank != 0:
+        return 0  # replicas only: rank 0 measures
+    build_library()
+    dev = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    h = qgemv.create(0)
+    M = args.prefill
+    stream = torch.cuda.Stream(device=dev)
+    rows, total_flop, total_ms, launches = [], 0.0, 0.0, 0
+    clocks = Clocks(0, str(getattr(props, "uuid", "")) or None)
+    for lab, N, K in shapes:
+        W = torch.from_numpy(synth.make_weights(synth.NVFP4, N, K, synth.config_seed(1, 0))).to(dev)
+        X = torch.from_numpy(np.stack([synth.make_x(synth.NVFP4, K, 11 + 7919 * m) for m in range(M)])
+                             .view(np.int16)).to(dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        copies = max(2, math.ceil(3 * l2 / (W.numel() + X.numel() * 2)))
+        Ws = [W] + [W.clone() for _ in range(copies - 1)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                qgemv.run_gemm(h, synth.NVFP4, X, M, Ws[i % copies], N, K, Y, stream=stream)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                qgemv.run_gemm(h, synth.NVFP4, X, M, Ws[i % copies], N, K, Y, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        st = qgemv.check_error(h, stream)
+        if st != qgemv.OK:
+            raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
+        ms = e0.elapsed_time(e1)
+        flop = 2.0 * M * N * K * args.steps
+        rows.append({"gemm": f"{lab}:NVFP4:{M}x{N}x{K}", "us": ms * 1e3 / args.steps,
+                     "TFLOP/s": flop / (ms * 1e-3) / 1e12, "copies": copies})
+        total_flop += flop
+        total_ms += ms
+        launches += args.steps
+        del Ws, W, X, Y
+    clk = clocks.stop()
+    peak, kind = load_bf16_peak()
+    value = total_flop / (total_ms * 1e-3) / 1e12
+    line = {"metric": "NVFP4 W4A16 prefill GEMM TFLOP/s (qgemv_run_gemm)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "replicas only", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "impl": "ours",
+            "config": {"workload": args.workload, "rows": M, "gemms": rows,
+                       "timing": "CUDA events around --steps launches per matrix, rotating weight copies"},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                         "frac": value / peak, "peak_kind": f"bf16_tflops of {kind} (dense bf16 burst)",
+                         "traffic": None},
+            "gpu_launches": launches, "clocks": clk, "build": qgemv.build_marker(), "gpu": props.name}
+    print(json.dumps(line), flush=True)
+    h.close()
+    return 0
+
+
+def run_profile_prefill(args, gemvs):
+    """`--prefill M --profile-launches N`: N plain GEMM launches per NVFP4 matrix, for a profiler."""
+    import torch
+
+    from quantized_weight_dequant_gb300 import qgemv
+    from quantized_weight_dequant_gb300.build import build_library
+
+    build_library()
+    h = qgemv.create(0)
+    M = args.prefill
+    for lab, f, N, K, _ in gemvs:
+        if f != synth.NVFP4 or args.only not in (None, lab):
+            continue
+        W = torch.from_numpy(synth.make_weights(f, N, K, synth.config_seed(1, 0))).cuda()
+        X = torch.from_numpy(np.stack([synth.make_x(f, K, 11 + 7919 * m) for m in range(M)]).view(np.int16)).cuda()
+        Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        for _ in range(args.profile_launches):
+            qgemv.run_gemm(h, f, X, M, W, N, K, Y)
+        torch.cuda.synchronize()
+        st = qgemv.check_error(h)
+        if st != qgemv.OK:
+            raise RuntimeError(f"qgemv error {qgemv.status_string(st)}")
+        print(f"{lab}: {args.profile_launches} GEMM launches of {M}x{N}x{K}", flush=True)
+    h.close()
+    return 0
+
+
 def run_ours(args, gemvs, rank, world):
     import torch
 
@@ -541,6 +648,8 @@ def main(argv=None):
     ap.add_argument("--only", default=None, help="with --profile-launches: the one GEMV label to run")
     ap.add_argument("--batch", type=int, default=1,
                     help="activation vectors per GEMV (1..8; > 1 runs qgemv_run_batch, ungrouped workloads only)")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="M > 0: time the NVFP4 GEMM of M activation rows (the prefill path) instead of the GEMV")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, when known for this build")
     args = ap.parse_args(argv)
@@ -553,8 +662,17 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     gemvs = WORKLOADS[args.workload]
+    if args.prefill < 0:
+        ap.error("--prefill must be >= 0")
+    if args.prefill and args.profile_launches:
+        return run_profile_prefill(args, gemvs)
     if args.profile_launches:
         return run_profile_launches(args, gemvs)
+    if args.prefill:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "--prefill has no oracle arm: the oracle is a GEMV"}))
+            return 0
+        return run_prefill(args, gemvs, rank, world)
     if args.impl == "reference":
         return run_reference(args, gemvs, rank, world)
     return run_ours(args, gemvs, rank, world)

@@ -34,3 +34,10 @@ def test_swiglu_group_must_hold_two_matrices(monkeypatch):
     monkeypatch.setitem(bench.GROUPS, "q4k_llama8b_decode", {"qkv": "mlp"})
     with pytest.raises(ValueError):
         bench.launch_units("q4k_llama8b_decode", bench.WORKLOADS["q4k_llama8b_decode"])
+
+
+def test_prefill_option_is_validated():
+    """--prefill takes a row count >= 0; the oracle arm has no prefill measurement."""
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--prefill", "-1"])
