@@ -48,7 +48,7 @@ constexpr int kTcBK = 64;           // K per stage
 constexpr int kTcGroupWarps = 8;    // dequantising warps per group (two groups: even and odd stages)
 constexpr int kTcThreads = 32 * (2 + 2 * kTcGroupWarps);
 constexpr int kTcRawDepth = 4;      // raw stages per group
-constexpr int kTcRaw = kTcRows * 32 + 2 * kTcRows * 4;  // codes [128][32 B], scales [half][128][4 B]
+constexpr int kTcRaw = kTcRows * 32 + 2 * kTcRows * 4;  // codes [half][128][16 B], scales [half][128][4 B]
 
 struct TcArgs {
   const uint8_t* W;  // e2m1 codes [N, K/2], low nibble first
@@ -274,7 +274,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
     const bool rv = n < a.N;
     const uint8_t* wrow = a.W + (rv ? n : 0) * static_cast<int64_t>(a.K / 2) + 16 * hh;
     const uint8_t* srow = a.S + (rv ? n : 0) * static_cast<int64_t>(a.K / 16);
-    const uint32_t rq = static_cast<uint32_t>(r * 32 + 16 * hh);
+    // raw slot: codes [half][row][16 B] (a warp's 32 rows of one half are 512 contiguous bytes),
+    // scales [half][row][4 B]
+    const uint32_t rq = static_cast<uint32_t>((hh * kTcRows + r) * 16);
     const uint32_t rsc = static_cast<uint32_t>(kTcRows * 32 + (hh * kTcRows + r) * 4);
     const uint32_t ring = rs0 + static_cast<uint32_t>(g * RD) * kTcRaw;
     const uint32_t lane_a = tmem + (static_cast<uint32_t>(32 * q4) << 16) + BT + 16 * hh;
