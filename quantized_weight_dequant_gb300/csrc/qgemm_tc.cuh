@@ -180,12 +180,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t xs0 = base;                                 // X stages: BT rows x 128 bytes
   const uint32_t rs0 = base + kTcStages * BT * 128;          // raw stages: [group][RD]
-  const uint32_t bars = rs0 + 2 * RD * kTcRaw;               // full_x[S], full_w[S], empty[S], accum
-  const uint32_t accum = bars + 8 * 3 * kTcStages;
+  const uint32_t bars = rs0 + 2 * RD * kTcRaw;               // full[S], empty[S], accum
+  const uint32_t accum = bars + 8 * 2 * kTcStages;
   const uint32_t tslot = accum + 8;                          // TMEM base written by tcgen05.alloc
-  auto full_x = [&](int s) { return bars + 8u * s; };
-  auto full_w = [&](int s) { return bars + 8u * (kTcStages + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * kTcStages + s); };
+  // full[s]: the X copy (one arrival with its transaction bytes) and the stage's 256
+  // dequantising threads; empty[s]: the MMAs that read stage s have completed
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (kTcStages + s); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // block = (weight tile, token tile, split): the splits of a tile form one cluster
@@ -206,8 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(full_x(s), 1);
-      mbar_init(full_w(s), kTcGroupWarps * 32);
+      mbar_init(full(s), 1 + kTcGroupWarps * 32);
       mbar_init(empty(s), 1);
     }
     mbar_init(accum, 1);
@@ -233,12 +233,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(full_x(s), BT * 128);
-        tma_load_2d(xs0 + s * BT * 128, &xmap, kb_at(i) * kTcBK, t0, full_x(s));
+        mbar_arrive_expect_tx(full(s), BT * 128);
+        tma_load_2d(xs0 + s * BT * 128, &xmap, kb_at(i) * kTcBK, t0, full(s));
       }
-      // the copies issued last have landed before the CTA may leave
+      // the copies issued last have landed before the CTA may leave (their stages' full phases
+      // complete once the copy and the stage's dequantisers are in)
       for (int j = i > kTcStages ? i - kTcStages : 0; j < i; ++j)
-        if (!mbar_wait_bounded(full_x(j % kTcStages), (j / kTcStages) & 1, a.spin_ns)) ok = false;
+        if (!mbar_wait_bounded(full(j % kTcStages), (j / kTcStages) & 1, a.spin_ns)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issue
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
       int s = 0;
       uint32_t ph = 0;
       for (int i = 0; i < nkb; ++i) {
-        if (!mbar_wait_bounded(full_x(s), ph, a.spin_ns) || !mbar_wait_bounded(full_w(s), ph, a.spin_ns)) {
+        if (!mbar_wait_bounded(full(s), ph, a.spin_ns)) {
           ok = false;
           break;
         }
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
       tmem_st16(lane_a + 32 * s, v);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(full_w(s));
+      mbar_arrive(full(s));
     }
     cp_async_wait<0>();
 
