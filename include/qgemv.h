@@ -151,7 +151,10 @@ int qgemv_group_size(qgemv_format_t fmt);
  *                             streaming launch also wait on a barrier that nothing completes,
  *                             bounded by the spin limit, so the timeout path (error word,
  *                             draining of in-flight copies, QGEMV_ERR_TIMEOUT from
- *                             qgemv_check_error) can be exercised without hanging a GPU.
+ *                             qgemv_check_error) can be exercised without hanging a GPU; in
+ *                             qgemv_run_gemm's tensor-core kernel, the first CTA's
+ *                             dequantising threads withhold their arrival for its first stage,
+ *                             so its MMA, copy and dequantising waits all run out.
  *   QGEMV_OPT_CTAS_PER_SM     streaming kernel CTAs per SM, 1 or 2 (default 2, used when
  *                             a row needs at most 8 warps); with 1, each CTA takes about half
  *                             an SM, so the next kernel of a programmatic-dependent-launch

@@ -60,6 +60,7 @@ struct TcArgs {
   int ks, kb_per;    // K splits per tile (the cluster size) and 64-wide K-blocks per split
   int* err;
   uint64_t spin_ns;
+  int stall;         // test hook: CTA 0's dequantisers withhold their arrival for its first stage
 };
 
 // Stages (X in shared memory, A in TMEM): eight, five for 256-token tiles (shared memory).
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
       tmem_st16(lane_a + 32 * s, v);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(full(s));
+      if (!(a.stall && blockIdx.x == 0 && i == 0)) mbar_arrive(full(s));
     }
     cp_async_wait<0>();
 

@@ -100,7 +100,6 @@ struct Problem {
   void* y = nullptr;
   float alpha = 1.f, beta = 0.f;
   int ydt = 0, pair = 0;
-  bool plain() const { return alpha == 1.f && beta == 0.f && ydt == 0 && !pair; }
 };
 
 struct Plan {
@@ -824,6 +823,7 @@ qgemv_status_t qgemv_run_gemm(qgemv_handle_t hh, qgemv_format_t fmt, const void*
   a.kb_per = static_cast<int>(kb_per);
   a.err = h->err;
   a.spin_ns = h->spin_ns;
+  a.stall = h->test_stall;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * ks), 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);

@@ -126,3 +126,24 @@ def test_gemm_rejects_bad_arguments(h):
     assert qgemv.run_gemm(h, synth.NVFP4, x, 16, W, N, 1000, y, check=False) == qgemv.ERR_BAD_SHAPE
     torch.cuda.synchronize()
     assert qgemv.check_error(h) == qgemv.OK
+
+
+def test_tensor_core_gemm_wait_times_out_and_the_context_stays_usable(h):
+    """The test hook withholds one stage's arrivals in the first CTA: its bounded waits run out,
+    the error word reports QGEMV_ERR_TIMEOUT, and the next call is correct."""
+    fmt, N, K, M = synth.NVFP4, 256, 1024, 32
+    W = synth.make_weights(fmt, N, K, seed=9)
+    Wd, _ = dev_bytes(W)
+    X = _xs(fmt, M, K, seed=9)
+    qgemv.set_option(h, qgemv.OPT_SPIN_LIMIT_NS, 2_000_000)
+    qgemv.set_option(h, qgemv.OPT_TEST_STALL, 1)
+    try:
+        _run(h, fmt, X, Wd, N, K)
+        assert qgemv.check_error(h) == qgemv.ERR_TIMEOUT
+    finally:
+        qgemv.set_option(h, qgemv.OPT_TEST_STALL, 0)
+        qgemv.set_option(h, qgemv.OPT_SPIN_LIMIT_NS, 1_000_000_000)
+    assert qgemv.check_error(h) == qgemv.OK
+    Y = _run(h, fmt, X, Wd, N, K)
+    _check(Y, X, fmt, W, N, K, range(M), "after timeout")
+    assert qgemv.check_error(h) == qgemv.OK
