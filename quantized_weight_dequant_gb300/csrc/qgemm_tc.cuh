@@ -4,7 +4,7 @@
 //
 // The weights are block-scaled FP4 and the activations bf16.  A block-scaled FP4 MMA would
 // need the activations in FP4 too, which changes the result; instead the weights are
-// dequantised into the MMA's operand tile in shared memory.  e2m1 times an e4m3 scale has at
+// dequantised into the MMA's A operand in tensor memory.  e2m1 times an e4m3 scale has at
 // most 6 significant bits and lies within [2^-10, 2688], so the bf16 operand is the exact
 // weight and the tensor core's fp32 accumulation is the only rounding.
 //
@@ -18,16 +18,18 @@
 //    finishes first).
 //  * Warp 0: allocates TMEM, then one lane loads the X tile of each stage with a 2-D TMA copy
 //    (rows past T read as zeros).  Warp 1: one lane issues tcgen05.mma (four K = 16 steps per
-//    stage) and frees each stage with tcgen05.commit.  Warps 2..17 dequantise in two groups of
-//    eight that take the even and the odd stages: the thread of TMEM lane r and half hh copies
-//    its 16 bytes of codes and the row's 4 scale bytes of each of its stages into a private
-//    ring with cp.async (three stages ahead), then writes the 32 weights as bf16 pairs into the
-//    stage's A columns with tcgen05.st.  Afterwards the 16 warps read the accumulator with
-//    tcgen05.ld (each its TMEM lane quarter and a quarter of the columns).
+//    stage) once the stage's one full barrier has the X copy's bytes and the arrivals of its
+//    256 dequantising threads, and frees the stage with tcgen05.commit.  Warps 2..17
+//    dequantise in two groups of eight that take the even and the odd stages: the thread of
+//    TMEM lane r and half hh copies its 16 bytes of codes and the row's 4 scale bytes of each
+//    of its stages into a private ring with cp.async (three stages ahead), then writes the 32
+//    weights as bf16 pairs into the stage's A columns with tcgen05.st.  Afterwards the 16
+//    warps read the accumulator with tcgen05.ld (each its TMEM lane quarter and a quarter of
+//    the columns).
 //  * Shared memory carries only X and the raw codes: the weights never round-trip through it.
-//  * Each CTA starts its K loop at its own offset, so that concurrent CTAs spread their X
-//    requests over L2 (all of them asking for the same K-block of X at once queues the TMA
-//    loads for thousands of cycles).
+//  * Each CTA starts its K loop at its own offset, so that concurrent CTAs ask for different
+//    K-blocks of X (no measured change on the shapes timed, where the MMA-issuing thread's
+//    loop is the limit; it costs nothing).
 //  * Every wait on an mbarrier is bounded; a wait that gives up sets the error word, and the
 //    CTA still waits for its copies and MMAs and frees its TMEM before it returns.
 #pragma once
@@ -199,9 +201,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   const int64_t n0 = static_cast<int64_t>(wt) * kTcRows;
   const int kb0 = ksi * a.kb_per;
   const int nkb = min(a.K / kTcBK - kb0, a.kb_per);  // K-blocks of this CTA (>= 1)
-  // The CTA walks its K-blocks from a rotated start: CTAs that run at the same time then ask
-  // for different K-blocks of X (and of the weight tiles that token tiles share) instead of
-  // queueing on the same L2 lines.  The order is fixed per CTA, so results are reproducible.
+  // The CTA walks its K-blocks from a rotated start, so CTAs that run at the same time ask for
+  // different K-blocks of X and of the weight tiles that token tiles share.  The order is
+  // fixed per CTA, so results are reproducible.
   const int rot = static_cast<int>((static_cast<unsigned>(wt) * 17u + static_cast<unsigned>(tt) * 5u) %
                                    static_cast<unsigned>(nkb));
   auto kb_at = [&](int i) { return kb0 + (i + rot < nkb ? i + rot : i + rot - nkb); };
