@@ -274,12 +274,13 @@ qgemv_status_t qgemv_run_batch(qgemv_handle_t h, qgemv_format_t fmt, const void*
  * Y = X . dequant(W)^T for any number M >= 1 of activation rows: the matrix-matrix product
  * that the Mojo "fp4_gemv" page sets beside its GEMV (its opening description: a whole prompt
  * goes through the prefill path, a shared-memory tile feeding the matrix unit, while decode
- * at M = 1 is the GEMV).  NVFP4 with M > QGEMV_MAX_BATCH and K a multiple of 64 runs on the
- * fifth-generation tensor cores (tcgen05): tiles of 128 weight rows x 256 (M <= 128: 128)
- * rows of X, X brought in by TMA, the weights dequantised exactly to bf16 into the
- * shared-memory operand tile (e2m1 times an e4m3 scale has at most 6 significant bits), fp32
- * accumulation in tensor memory.  Every other call goes through qgemv_run_batch in chunks of
- * QGEMV_MAX_BATCH rows.
+ * at M = 1 is the GEMV).  NVFP4 with M > QGEMV_MAX_BATCH runs on the fifth-generation tensor
+ * cores (tcgen05) when K is a multiple of 128 (of 64 when M > 128): tiles of 128 weight rows x
+ * 64, 128 or 256 rows of X (by M), X brought in by TMA, the weights dequantised exactly to
+ * bf16 into the MMA's A operand in tensor memory (e2m1 times an e4m3 scale has at most 6
+ * significant bits), fp32 accumulation in tensor memory, K split over a thread-block cluster
+ * when the tiles do not fill the GPU.  Every other call goes through qgemv_run_batch in
+ * chunks of QGEMV_MAX_BATCH rows.
  *
  * x: device, M rows of K 16-bit values (fp16; bf16 for NVFP4), row-major, 16-byte aligned.
  * y: device, M rows of N fp32 values, row-major (y[m * N + n]), 16-byte aligned.

@@ -8,21 +8,22 @@
 // most 6 significant bits and lies within [2^-10, 2688], so the bf16 operand is the exact
 // weight and the tensor core's fp32 accumulation is the only rounding.
 //
-//  * Tile: 128 weight rows (the MMA's M, TMEM lanes) x BT tokens (its N), in stages of 64
-//    along K.  D = W_tile . X_tile^T: the dequantised weights are the A operand in tensor
-//    memory (each lane a weight row, two bf16 per column), X the B operand in shared memory,
-//    K-major in the 128-byte swizzle layout.  When the tiles do not fill the GPU (few tokens),
+//  * Tile: 128 weight rows (the MMA's M, TMEM lanes) x BT tokens (its N), in stages of BK along
+//    K (128 for BT <= 128, 64 for BT = 256: shared memory).  D = W_tile . X_tile^T: the
+//    dequantised weights are the A operand in tensor memory (each lane a weight row, two bf16
+//    per column), X the B operand in shared memory, K-major in the 128-byte swizzle layout
+//    (BK / 64 sub-tiles of 128-byte rows).  When the tiles do not fill the GPU (few tokens),
 //    K is split over the ks CTAs of a thread-block cluster: each leaves its partial tile in its
 //    own shared memory, and CTA q of the cluster adds column slice q of all ks partials through
 //    distributed shared memory, in rank order (so the result does not depend on which CTA
 //    finishes first).
 //  * Warp 0: allocates TMEM, then one lane loads the X tile of each stage with a 2-D TMA copy
-//    (rows past T read as zeros).  Warp 1: one lane issues tcgen05.mma (four K = 16 steps per
+//    (rows past T read as zeros).  Warp 1: one lane issues tcgen05.mma (BK / 16 steps of K 16 per
 //    stage) once the stage's one full barrier has the X copy's bytes and the arrivals of its
 //    256 dequantising threads, and frees the stage with tcgen05.commit.  Warps 2..17
 //    dequantise in two groups of eight that take the even and the odd stages: the thread of
-//    TMEM lane r and half hh copies its 16 bytes of codes and the row's 4 scale bytes of each
-//    of its stages into a private ring with cp.async (three stages ahead), then writes the 32
+//    TMEM lane r and half hh copies its BK / 4 bytes of codes and 4 scale bytes of each of its
+//    stages into a private ring with cp.async (three stages ahead), then writes the BK / 2
 //    weights as bf16 pairs into the stage's A columns with tcgen05.st.  Afterwards the 16
 //    warps read the accumulator with tcgen05.ld (each its TMEM lane quarter and a quarter of
 //    the columns).
@@ -46,11 +47,9 @@
 namespace qg {
 
 constexpr int kTcRows = 128;        // weight rows per tile: the MMA's M and the TMEM lanes
-constexpr int kTcBK = 64;           // K per stage
 constexpr int kTcGroupWarps = 8;    // dequantising warps per group (two groups: even and odd stages)
 constexpr int kTcThreads = 32 * (2 + 2 * kTcGroupWarps);
-constexpr int kTcRawDepth = 4;      // raw stages per group
-constexpr int kTcRaw = kTcRows * 32 + 2 * kTcRows * 4;  // codes [half][128][16 B], scales [half][128][4 B]
+constexpr int kTcRawDepth = 4;      // raw stages per group (cp.async ring, three in flight)
 
 struct TcArgs {
   const uint8_t* W;  // e2m1 codes [N, K/2], low nibble first
@@ -59,18 +58,26 @@ struct TcArgs {
   int64_t N;
   int T, K;
   int n_ttiles;      // token tiles: ceil(T / BT)
-  int ks, kb_per;    // K splits per tile (the cluster size) and 64-wide K-blocks per split
+  int ks, kb_per;    // K splits per tile (the cluster size) and K-blocks (of tc_bk) per split
   int* err;
   uint64_t spin_ns;
   int stall;         // test hook: CTA 0's dequantisers withhold their arrival for its first stage
 };
 
-// Stages (X in shared memory, A in TMEM): eight, five for 256-token tiles (shared memory).
-__host__ __device__ constexpr int tc_stages(int BT) { return BT > 128 ? 5 : 8; }
-// TMEM columns: the accumulator [0, BT), A stage s at BT + 32 s (rounded up to a power of 2)
-__host__ __device__ constexpr int tc_tmem_cols(int BT) { return BT + tc_stages(BT) * 32 <= 256 ? 256 : 512; }
+// K per stage: 128 (two 128-byte swizzle rows of bf16, eight MMAs per barrier round trip) for
+// tiles of up to 128 tokens; 64 for 256-token tiles, whose X stages would not fit otherwise.
+__host__ __device__ constexpr int tc_bk(int BT) { return BT > 128 ? 64 : 128; }
+// Stages (X in shared memory, A in TMEM), within 227 KB of shared memory and 512 TMEM columns.
+__host__ __device__ constexpr int tc_stages(int BT) { return BT > 128 ? 5 : BT > 64 ? 4 : 6; }
+// Raw stage: codes [half][128 rows][BK / 4 bytes], scales [half][128 rows][4 bytes].
+__host__ __device__ constexpr int tc_raw_bytes(int BT) { return 2 * kTcRows * (tc_bk(BT) / 4) + 2 * kTcRows * 4; }
+// TMEM columns: the accumulator [0, BT), A stage s at BT + (BK / 2) s (a power of 2)
+__host__ __device__ constexpr int tc_tmem_cols(int BT) {
+  return BT + tc_stages(BT) * (tc_bk(BT) / 2) <= 256 ? 256 : 512;
+}
 __host__ __device__ constexpr size_t tc_smem_bytes(int BT) {
-  return 1024 + static_cast<size_t>(tc_stages(BT)) * BT * 128 + static_cast<size_t>(2 * kTcRawDepth) * kTcRaw + 256;
+  return 1024 + static_cast<size_t>(tc_stages(BT)) * BT * 2 * tc_bk(BT) +
+         static_cast<size_t>(2 * kTcRawDepth) * tc_raw_bytes(BT) + 256;
 }
 
 // ------------------------------------------------------------------ tcgen05 / TMA wrappers
@@ -179,11 +186,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   constexpr int TC = tc_tmem_cols(BT);
   constexpr int RD = kTcRawDepth;
   constexpr int kTcStages = tc_stages(BT);
+  constexpr int BK = tc_bk(BT), NSUB = BK / 64;    // K per stage, 128-byte swizzle rows per X row
+  constexpr int XSTAGE = BT * 2 * BK;               // bytes of an X stage: NSUB sub-tiles of BT x 128
+  constexpr int ACOLS = BK / 2;                     // TMEM columns of an A stage
+  constexpr int RAW = tc_raw_bytes(BT), CODES = BK / 4;  // raw stage bytes, code bytes per half row
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t xs0 = base;                                 // X stages: BT rows x 128 bytes
-  const uint32_t rs0 = base + kTcStages * BT * 128;          // raw stages: [group][RD]
-  const uint32_t bars = rs0 + 2 * RD * kTcRaw;               // full[S], empty[S], accum
+  const uint32_t xs0 = base;                                 // X stages: NSUB x BT rows x 128 bytes
+  const uint32_t rs0 = base + kTcStages * XSTAGE;            // raw stages: [group][RD]
+  const uint32_t bars = rs0 + 2 * RD * RAW;                  // full[S], empty[S], accum
   const uint32_t accum = bars + 8 * 2 * kTcStages;
   const uint32_t tslot = accum + 8;                          // TMEM base written by tcgen05.alloc
   // full[s]: the X copy (one arrival with its transaction bytes) and the stage's 256
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   const int t0 = tt * BT;
   const int64_t n0 = static_cast<int64_t>(wt) * kTcRows;
   const int kb0 = ksi * a.kb_per;
-  const int nkb = min(a.K / kTcBK - kb0, a.kb_per);  // K-blocks of this CTA (>= 1)
+  const int nkb = min(a.K / BK - kb0, a.kb_per);  // K-blocks of this CTA (>= 1)
   // The CTA walks its K-blocks from a rotated start, so CTAs that run at the same time ask for
   // different K-blocks of X and of the weight tiles that token tiles share.  The order is
   // fixed per CTA, so results are reproducible.
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = lds_u32(tslot);  // accumulator at column 0, A stage s at column BT + 32 s
+  const uint32_t tmem = lds_u32(tslot);  // accumulator at column 0, A stage s at BT + ACOLS s
   bool ok = true;
 
   if (warp == 0) {
@@ -236,8 +247,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(full(s), BT * 128);
-        tma_load_2d(xs0 + s * BT * 128, &xmap, kb_at(i) * kTcBK, t0, full(s));
+        mbar_arrive_expect_tx(full(s), XSTAGE);
+#pragma unroll
+        for (int u = 0; u < NSUB; ++u)
+          tma_load_2d(xs0 + s * XSTAGE + u * BT * 128, &xmap, kb_at(i) * BK + 64 * u, t0, full(s));
       }
       // the copies issued last have landed before the CTA may leave (their stages' full phases
       // complete once the copy and the stage's dequantisers are in)
@@ -247,8 +260,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issue
       constexpr uint32_t idesc = tc_idesc_bf16(kTcRows, BT);
-      // descriptor of stage 0; stage s and K-step k start (s BT 128 + 32 k) bytes later, which
-      // adds (s BT 8 + 2 k) to the start-address field (no carry: addresses stay below 2^18)
+      // descriptor of stage 0; K-step k of stage s starts at byte s XSTAGE + (k / 4) BT 128 +
+      // 32 (k % 4), a sixteenth of that added to the start-address field (no carry: addresses
+      // stay below 2^18)
       const uint64_t xd0 = tc_desc_sw128(xs0);
       int s = 0;
       uint32_t ph = 0;
@@ -258,12 +272,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
           break;
         }
         tc_fence_after();
-        const uint64_t xd = xd0 + static_cast<uint64_t>(s * BT * 8);
-        const uint32_t ta = tmem + BT + 32 * s;
-        tc_mma_bf16_ta(tmem, ta, xd, idesc, static_cast<uint32_t>(i));
-        tc_mma_bf16_ta(tmem, ta + 8, xd + 2, idesc, 1u);
-        tc_mma_bf16_ta(tmem, ta + 16, xd + 4, idesc, 1u);
-        tc_mma_bf16_ta(tmem, ta + 24, xd + 6, idesc, 1u);
+        const uint64_t xd = xd0 + static_cast<uint64_t>(s * (XSTAGE / 16));
+        const uint32_t ta = tmem + BT + ACOLS * s;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma_bf16_ta(tmem, ta + 8 * k, xd + static_cast<uint64_t>((k >> 2) * (BT * 8) + 2 * (k & 3)), idesc,
+                         k == 0 ? static_cast<uint32_t>(i) : 1u);
         tc_commit(empty(s));
         if (++s == kTcStages) s = 0, ph ^= 1;
       }
@@ -271,26 +285,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
     }
   } else {
     // ---- dequantisation: warp group g takes stages g, g + 2, ...; the thread of TMEM lane r
-    // (row r of the tile) and half hh writes A columns 16 hh .. 16 hh + 15 of each of them
+    // (row r of the tile) and half hh writes A columns hh BK / 4 .. (hh + 1) BK / 4 - 1 of each
     const int dw = warp - 2, q4 = warp & 3, hh = (dw >> 2) & 1, g = dw >> 3;
     const int r = 32 * q4 + lane;
     const int64_t n = n0 + r;
     const bool rv = n < a.N;
-    const uint8_t* wrow = a.W + (rv ? n : 0) * static_cast<int64_t>(a.K / 2) + 16 * hh;
-    const uint8_t* srow = a.S + (rv ? n : 0) * static_cast<int64_t>(a.K / 16);
-    // raw slot: codes [half][row][16 B] (a warp's 32 rows of one half are 512 contiguous bytes),
+    const uint8_t* wrow = a.W + (rv ? n : 0) * static_cast<int64_t>(a.K / 2) + CODES * hh;
+    // scales: BK = 128 takes the 4 bytes of its half (blocks 4 hh .. 4 hh + 3); BK = 64 the
+    // row's 4 bytes of the stage, of which its half uses 2
+    const uint8_t* srow = a.S + (rv ? n : 0) * static_cast<int64_t>(a.K / 16) + (BK == 128 ? 4 * hh : 0);
+    // raw slot: codes [half][row][CODES] (a warp's 32 rows of one half are contiguous),
     // scales [half][row][4 B]
-    const uint32_t rq = static_cast<uint32_t>((hh * kTcRows + r) * 16);
-    const uint32_t rsc = static_cast<uint32_t>(kTcRows * 32 + (hh * kTcRows + r) * 4);
-    const uint32_t ring = rs0 + static_cast<uint32_t>(g * RD) * kTcRaw;
-    const uint32_t lane_a = tmem + (static_cast<uint32_t>(32 * q4) << 16) + BT + 16 * hh;
+    const uint32_t rq = static_cast<uint32_t>((hh * kTcRows + r) * CODES);
+    const uint32_t rsc = static_cast<uint32_t>(2 * kTcRows * CODES + (hh * kTcRows + r) * 4);
+    const uint32_t ring = rs0 + static_cast<uint32_t>(g * RD) * RAW;
+    const uint32_t lane_a = tmem + (static_cast<uint32_t>(32 * q4) << 16) + BT + (ACOLS / 2) * hh;
     const int nj = (nkb - g + 1) / 2;  // this group's stages
     auto issue = [&](int j) {
-      const uint32_t slot = ring + static_cast<uint32_t>(j % RD) * kTcRaw;
+      const uint32_t slot = ring + static_cast<uint32_t>(j % RD) * RAW;
       if (j < nj && rv) {
         const int64_t kb = kb_at(g + 2 * j);
-        cp_async16(slot + rq, wrow + kb * 32);
-        cp_async4(slot + rsc, srow + kb * 4);
+#pragma unroll
+        for (int u = 0; u < CODES / 16; ++u) cp_async16(slot + rq + 16 * u, wrow + kb * (BK / 2) + 16 * u);
+        cp_async4(slot + rsc, srow + kb * (BK / 16));
       }
       cp_async_commit();
     };
@@ -306,23 +323,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_nvfp4_kernel(const __grid_co
       }
       tc_fence_after();  // the MMAs that read A stage s are complete
       cp_async_wait<RD - 1>();
-      const uint32_t slot = ring + static_cast<uint32_t>(j % RD) * kTcRaw;
-      uint4 qv = lds_v4(slot + rq);
-      uint32_t c = lds_u32(slot + rsc) >> (16 * hh);
-      if (!rv) qv = make_uint4(0u, 0u, 0u, 0u), c = 0;
-      const uint32_t s2 = DecNVFP4::e4m3x2(c & 0x7F7Fu);  // |scale| of blocks 2 hh, 2 hh + 1
-      const uint32_t S0 = __byte_perm(s2, s2, 0x1010), S1 = __byte_perm(s2, s2, 0x3232);
-      const uint32_t wv[4] = {qv.x, qv.y, qv.z, qv.w};
-      uint32_t v[16];
+      const uint32_t slot = ring + static_cast<uint32_t>(j % RD) * RAW;
+      uint32_t c = lds_u32(slot + rsc);
+      if (BK == 64) c >>= 16 * hh;  // the half's two scale bytes
+      if (!rv) c = 0;
+      // |scale| of the half's blocks as fp16 pairs (block b in both halves of sc[b])
+      uint32_t sc[CODES / 8];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {  // word w: elements 32 hh + 8 w .. + 8 = columns 16 hh + 4 w .. + 4
-        uint32_t hv[4];
-        DecNVFP4::e2m1x8(wv[w], hv);
-        const uint32_t sj = w < 2 ? S0 : S1;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[4 * w + u] = h2_to_bf2(tc_hmul2(hv[u], sj));
+      for (int b = 0; b < CODES / 8; b += 2) {
+        const uint32_t s2 = DecNVFP4::e4m3x2((c >> (8 * b)) & 0x7F7Fu);
+        sc[b] = __byte_perm(s2, s2, 0x1010);
+        sc[b + 1] = __byte_perm(s2, s2, 0x3232);
       }
-      tmem_st16(lane_a + 32 * s, v);
+#pragma unroll
+      for (int part = 0; part < CODES / 16; ++part) {  // 16 code bytes = 32 weights = 16 columns
+        uint4 qv = lds_v4(slot + rq + 16 * part);
+        if (!rv) qv = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t wv[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint32_t v[16];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {  // word w: 8 elements (columns 4 w .. 4 w + 3 of the part)
+          uint32_t hv[4];
+          DecNVFP4::e2m1x8(wv[w], hv);
+          const uint32_t sj = sc[2 * part + (w >> 1)];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[4 * w + u] = h2_to_bf2(tc_hmul2(hv[u], sj));
+        }
+        tmem_st16(lane_a + ACOLS * s + 16 * part, v);
+      }
       tmem_st_wait();
       tc_fence_before();
       if (!(a.stall && blockIdx.x == 0 && i == 0)) mbar_arrive(full(s));

@@ -775,8 +775,10 @@ qgemv_status_t qgemv_run_gemm(qgemv_handle_t hh, qgemv_format_t fmt, const void*
   if (!x || !y || M < 1) return QGEMV_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return QGEMV_ERR_MISALIGNED;
   const int f = static_cast<int>(fmt);
-  const bool tc = f == F_NVFP4 && M > QGEMV_MAX_BATCH && K % kTcBK == 0 && h->encode_tiled && h->force_path != 2 &&
-                  tc_smem_bytes(256) <= h->smem_optin;
+  const int BT = M > 128 ? 256 : M > 64 ? 128 : 64;
+  const int BK = tc_bk(BT);
+  const bool tc = f == F_NVFP4 && M > QGEMV_MAX_BATCH && K % BK == 0 && h->encode_tiled && h->force_path != 2 &&
+                  tc_smem_bytes(BT) <= h->smem_optin;
   if (!tc) {
     for (int64_t m0 = 0; m0 < M; m0 += QGEMV_MAX_BATCH) {
       const int mb = static_cast<int>(std::min<int64_t>(QGEMV_MAX_BATCH, M - m0));
@@ -786,14 +788,13 @@ qgemv_status_t qgemv_run_gemm(qgemv_handle_t hh, qgemv_format_t fmt, const void*
     return QGEMV_OK;
   }
   if (M > 0x7fffffff || K > 0x7fffffff) return QGEMV_ERR_BAD_SHAPE;
-  const int BT = M > 128 ? 256 : M > 64 ? 128 : 64;
   const int64_t ntt = (M + BT - 1) / BT, nwt = (N + kTcRows - 1) / kTcRows;
   if (ntt * nwt > 0x7fffffff) return QGEMV_ERR_BAD_SHAPE;
   // X as a 2-D tensor (K innermost, M rows), read in boxes of 64 x BT with the 128-byte swizzle
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(BT)};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BT)};  // one 128-byte swizzle row
   const cuuint32_t estr[2] = {1, 1};
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
                                 const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -805,7 +806,7 @@ qgemv_status_t qgemv_run_gemm(qgemv_handle_t hh, qgemv_format_t fmt, const void*
     return QGEMV_ERR_CUDA;
   // Split K over the CTAs of a cluster when the tiles fill fewer than all SMs: as many splits
   // as whole waves of tiles fit, at least four K-blocks each, at most the largest cluster.
-  const int64_t tiles = ntt * nwt, nk = K / kTcBK;
+  const int64_t tiles = ntt * nwt, nk = K / BK;
   int64_t ks = 1;
   if (tiles < h->sms)
     ks = std::min<int64_t>({h->sms / tiles, std::max<int64_t>(1, nk / 4), h->tc_cluster_max[BT > 128 ? 2 : BT > 64 ? 1 : 0]});

@@ -51,10 +51,11 @@ def _check(Y, X, fmt, W, N, K, ms, what):
 
 
 # (N, K, M): one K-block; ragged N and M; 129 rows (a 256-row tile, mostly outside X); long K
-# at M = 64 (128-row tiles, 56 K splits); K-blocks not a multiple of the ring depth; a full
-# prefill shape (2 splits); tiles enough for every SM (no split)
-TC_CASES = [(128, 64, 9), (200, 4096, 300), (1000, 2048, 129), (256, 14336, 64), (333, 960, 77),
-            (4096, 4096, 512), (130, 1024, 1000), (4096, 1024, 1100)]
+# at M = 64 (64-row tiles, 128-wide stages, 8 K splits); K-blocks not a multiple of the ring
+# depth (128- and 64-wide stages); a full prefill shape (2 splits); tiles enough for every SM
+# (no split)
+TC_CASES = [(128, 128, 9), (200, 4096, 300), (1000, 2048, 129), (256, 14336, 64), (333, 1152, 77),
+            (200, 960, 150), (4096, 4096, 512), (130, 1024, 1000), (4096, 1024, 1100)]
 
 
 @pytest.mark.parametrize("N,K,M", TC_CASES)
@@ -70,7 +71,8 @@ def test_tensor_core_gemm_matches_oracle(h, N, K, M):
     assert qgemv.check_error(h) == qgemv.OK
 
 
-@pytest.mark.parametrize("fmt,N,K,M", [(synth.NVFP4, 50, 4016, 20), (synth.Q4_K, 300, 4096, 20),
+@pytest.mark.parametrize("fmt,N,K,M", [(synth.NVFP4, 50, 4016, 20), (synth.NVFP4, 60, 960, 40),
+                                       (synth.Q4_K, 300, 4096, 20),
                                        (synth.TQ1_0, 64, 4096, 11), (synth.Q8_0, 40, 1280, 9),
                                        (synth.NVFP4, 96, 2048, 8), (synth.NVFP4, 64, 512, 1)])
 def test_gemm_batch_path(h, fmt, N, K, M):
