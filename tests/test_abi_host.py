@@ -76,6 +76,11 @@ def test_null_handle_and_pointer_arguments_are_rejected_without_a_launch():
     assert L.qgemv_set_option(None, 0, 0) == qgemv.ERR_INVALID_ARG
     assert L.qgemv_create(None, 0) == qgemv.ERR_INVALID_ARG
     assert L.qgemv_destroy(None) == qgemv.OK
+    # the layer, batch and many-row entry points check the handle first as well
+    assert L.qgemv_run_ex(None, 0, 16, 16, 4, 256, 1.0, 0.0, 16, 0, None) == qgemv.ERR_INVALID_ARG
+    assert L.qgemv_run_group(None, 16, 256, 1, None, None) == qgemv.ERR_INVALID_ARG
+    assert L.qgemv_run_batch(None, 0, 16, 2, 16, 4, 256, 16, None) == qgemv.ERR_INVALID_ARG
+    assert L.qgemv_run_gemm(None, 1, 16, 32, 16, 4, 256, 16, None) == qgemv.ERR_INVALID_ARG
 
 
 def test_create_reports_no_device_when_there_is_none():
