@@ -549,6 +549,41 @@ def run_ours(args, gemvs, rank, world):
         if label not in grouped:
             per_call[label]["plan"] = qgemv.describe(h, gemvs[idx[0]][1], gemvs[idx[0]][2], gemvs[idx[0]][3])
         del gg
+    if args.dense_context and B == 1:
+        # Context only (a library, not this product): the same GEMV with dense bf16 weights
+        # through cuBLAS (torch.mv), same protocol (graph of 200 launches over rotating copies
+        # that exceed L2), and the speed-up of the packed format over it.
+        for ui, (label, idx, sw) in enumerate(units):
+            if label in grouped:
+                continue
+            _, fmt, N, K, _ = gemvs[idx[0]]
+            dc = max(2, math.ceil(3 * l2 / (2 * N * K)))
+            Wb = [torch.randn(N, K, device=dev, dtype=torch.bfloat16) * 0.02 for _ in range(dc)]
+            xb = torch.randn(K, device=dev, dtype=torch.bfloat16)
+            with torch.cuda.stream(stream):
+                torch.mv(Wb[0], xb)  # cuBLAS sets up its handle outside the capture
+            stream.synchronize()
+            R = 200
+            gg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gg, stream=stream):
+                for i in range(R):
+                    torch.mv(Wb[i % dc], xb)
+            with torch.cuda.stream(stream):
+                gg.replay()
+            stream.synchronize()
+            samples = []
+            for _ in range(7):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    gg.replay()
+                    b.record(stream)
+                stream.synchronize()
+                samples.append(a.elapsed_time(b) * 1e3 / R)
+            dus = statistics.median(samples)
+            per_call[label]["dense_bf16_cublas_us"] = dus
+            per_call[label]["speedup_over_dense_bf16"] = dus / per_call[label]["us"]
+            del gg, Wb
     dom = max(units, key=lambda u_: unit_bytes(gemvs, u_[1], u_[2], B))[0]
     peak, peak_kind = load_peaks()
     achieved = per_call[dom]["GB/s"]
@@ -648,6 +683,8 @@ def main(argv=None):
     ap.add_argument("--only", default=None, help="with --profile-launches: the one GEMV label to run")
     ap.add_argument("--batch", type=int, default=1,
                     help="activation vectors per GEMV (1..8; > 1 runs qgemv_run_batch, ungrouped workloads only)")
+    ap.add_argument("--dense-context", action="store_true",
+                    help="also time each GEMV with dense bf16 weights through cuBLAS (context only)")
     ap.add_argument("--prefill", type=int, default=0,
                     help="M > 0: time the NVFP4 GEMM of M activation rows (the prefill path) instead of the GEMV")
     ap.add_argument("--traffic", type=float, default=None,
