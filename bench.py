@@ -433,7 +433,7 @@ def run_ours(args, gemvs, rank, world):
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
     step_w_bytes = sum(synth.packed_bytes(f, n, k) for _, f, n, k, _ in gemvs)
     copies = max(2, math.ceil(3 * l2 / step_w_bytes))
-    xs, Ws, ys, xbits = {}, [], [], {}
+    xs, Ws, ys = {}, [], []
     B = args.batch  # activation vectors per GEMV
     for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
         seed = synth.config_seed(1, gi) + 100 * rank
@@ -442,10 +442,26 @@ def run_ours(args, gemvs, rank, world):
         Ws.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
         if (xk, K, fmt) not in xs:
             xb = np.stack([synth.make_x(fmt, K, seed + 7919 * m) for m in range(B)])  # [B, K]
-            xbits[(xk, K, fmt)] = xb
             xs[(xk, K, fmt)] = torch.from_numpy(xb.view(np.int16).copy()).to(dev)
         ys.append(torch.empty((B, N), dtype=torch.float32, device=dev))
         del W
+    # Every x of a step in one device buffer and every output in another (views at 16-byte
+    # offsets), so the end-to-end run moves a step's inputs and results with one copy each way.
+    xoff, off = {}, 0
+    for k in xs:
+        xoff[k] = off
+        off += (xs[k].numel() + 7) // 8 * 8
+    xall = torch.zeros(off, dtype=torch.int16, device=dev)
+    for k in list(xs):
+        v = xall[xoff[k]:xoff[k] + xs[k].numel()].view(xs[k].shape)
+        v.copy_(xs[k])
+        xs[k] = v
+    yoff, off = [], 0
+    for y in ys:
+        yoff.append(off)
+        off += (y.numel() + 3) // 4 * 4
+    yall = torch.empty(off, dtype=torch.float32, device=dev)
+    ys = [yall[o:o + y.numel()].view(y.shape) for o, y in zip(yoff, ys)]
     units = launch_units(args.workload, gemvs)
     grouped = set(GROUPS.get(args.workload, {}).values())
     for label, idx, sw in units:
@@ -595,29 +611,48 @@ def run_ours(args, gemvs, rank, world):
                 "achieved_how": "algorithmic bytes per launch / mean launch duration over graph replays of 200 "
                                 "launches rotating weight copies (CUDA events on the launch stream)"}
 
-    # End to end through the public API: pinned host x -> device, 3 GEMVs, y -> pinned host.
+    # End to end through the public API: the step's packed x from pinned host memory to the
+    # device (one copy), one qgemv call per launch unit, the packed outputs back (one copy).
     e2e_steps = min(args.steps, 2000)
-    hx = {k: torch.from_numpy(v.view(np.int16).copy()).pin_memory() for k, v in xbits.items()}
-    outs = [y for y in ys if y is not None]
-    hy = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in outs]
-    h2d = sum(2 * v.size for v in xbits.values())
-    d2h = sum(4 * y.numel() for y in outs)
+    hx = torch.empty(xall.shape, dtype=torch.int16).pin_memory()
+    hx.copy_(xall.cpu())
+    hy = torch.empty(yall.shape, dtype=torch.float32).pin_memory()
+    h2d = 2 * xall.numel()
+    d2h = 4 * yall.numel()
+    def e2e_step(i):
+        xall.copy_(hx, non_blocking=True)
+        step(i, stream)
+        hy.copy_(yall, non_blocking=True)
+
+    # The steps are recorded in a CUDA graph, as a decode loop would run them: every replayed
+    # step still copies its inputs in and its results out (memcpy nodes), without the host's
+    # per-call launch cost.  If the copies cannot be captured the steps run eagerly.
+    e2e_spg = largest_divisor_le(e2e_steps, 20)
     with torch.cuda.stream(stream):
         for i in range(5):
-            for k in hx:
-                xs[k].copy_(hx[k], non_blocking=True)
-            step(i, stream)
-            for y, hyy in zip(outs, hy):
-                hyy.copy_(y, non_blocking=True)
+            e2e_step(i)
+    stream.synchronize()
+    ge = None
+    try:
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=stream):
+            for i in range(e2e_spg):
+                e2e_step(i)
+        with torch.cuda.stream(stream):
+            ge.replay()
         stream.synchronize()
+    except RuntimeError:
+        ge = None
+        torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for i in range(e2e_steps):
-            for k in hx:
-                xs[k].copy_(hx[k], non_blocking=True)
-            step(i, stream)
-            for y, hyy in zip(outs, hy):
-                hyy.copy_(y, non_blocking=True)
+        if ge is not None:
+            for _ in range(e2e_steps // e2e_spg):
+                ge.replay()
+        else:
+            for i in range(e2e_steps):
+                e2e_step(i)
         b.record(stream)
     stream.synchronize()
     e2e_ms = a.elapsed_time(b)
@@ -625,8 +660,9 @@ def run_ours(args, gemvs, rank, world):
     e2e = {"value": whole_job_gbs(world, e2e_steps, step_bytes, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "ms_per_step": e2e_ms / e2e_steps,
-           "how": "stream-ordered: pinned x H2D, one qgemv_run / qgemv_run_group per launch unit, "
-                  "outputs D2H per step; weights resident"}
+           "how": ("CUDA graph of %d steps, replayed" % e2e_spg if ge is not None else "eager, stream-ordered")
+                  + ": per step one pinned H2D copy of the step's packed x, one qgemv_run / qgemv_run_group / "
+                  "qgemv_run_batch per launch unit, one D2H copy of the packed outputs; weights resident"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
