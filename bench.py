@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +50,7 @@ for _p, _n, _k in synth.LAYER_SHAPES:
     for _f in (synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.Q8_0):
         WORKLOADS[f"layer_{_p}_{synth.FORMAT_NAMES[_f]}"] = [(_p, _f, _n, _k, "h")]
 DEFAULT_WORKLOAD = "q4k_llama8b_decode"
+WEIGHT_SEED = 1000  # seed of a workload's first weight matrix; matrix i takes WEIGHT_SEED + i
 
 # Layer launches: GEMVs of a workload that carry the same group tag run as ONE
 # qgemv_run_group launch (they share x); a group listed in SWIGLU holds a gate and an up
@@ -114,7 +116,7 @@ class Clocks:
 
     def __init__(self, device_index: int, uuid: str | None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"qgemv_clocks_{os.getpid()}.csv")
         target = f"GPU-{uuid}" if uuid else str(device_index)
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -276,11 +278,11 @@ def run_profile_launches(args, gemvs):
         Ws, ys = [], []
         for gi in idx:
             _, fmt, N, K, _ = gemvs[gi]
-            Ws.append(torch.from_numpy(synth.make_weights(fmt, N, K, synth.config_seed(1, gi))).cuda())
+            Ws.append(torch.from_numpy(synth.make_weights(fmt, N, K, WEIGHT_SEED + gi)).cuda())
             ys.append(torch.empty(N, dtype=torch.float32, device="cuda"))
         _, fmt, N, K, _ = gemvs[idx[0]]
         B = args.batch
-        x = torch.from_numpy(np.stack([synth.make_x(fmt, K, synth.config_seed(1, idx[0]) + 7919 * m)
+        x = torch.from_numpy(np.stack([synth.make_x(fmt, K, WEIGHT_SEED + idx[0] + 7919 * m)
                                        for m in range(B)]).view(np.int16)).cuda()
         if B > 1:
             ys = [torch.empty((B, gemvs[gi][2]), dtype=torch.float32, device="cuda") for gi in idx]
@@ -338,7 +340,7 @@ def run_prefill(args, gemvs, rank, world):
     rows, total_flop, total_ms, launches = [], 0.0, 0.0, 0
     clocks = Clocks(0, str(getattr(props, "uuid", "")) or None)
     for lab, N, K in shapes:
-        W = torch.from_numpy(synth.make_weights(synth.NVFP4, N, K, synth.config_seed(1, 0))).to(dev)
+        W = torch.from_numpy(synth.make_weights(synth.NVFP4, N, K, WEIGHT_SEED)).to(dev)
         X = torch.from_numpy(np.stack([synth.make_x(synth.NVFP4, K, 11 + 7919 * m) for m in range(M)])
                              .view(np.int16)).to(dev)
         Y = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -397,7 +399,7 @@ def run_profile_prefill(args, gemvs):
     for lab, f, N, K, _ in gemvs:
         if f != synth.NVFP4 or args.only not in (None, lab):
             continue
-        W = torch.from_numpy(synth.make_weights(f, N, K, synth.config_seed(1, 0))).cuda()
+        W = torch.from_numpy(synth.make_weights(f, N, K, WEIGHT_SEED)).cuda()
         X = torch.from_numpy(np.stack([synth.make_x(f, K, 11 + 7919 * m) for m in range(M)]).view(np.int16)).cuda()
         Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         for _ in range(args.profile_launches):
@@ -436,7 +438,7 @@ def run_ours(args, gemvs, rank, world):
     xs, Ws, ys = {}, [], []
     B = args.batch  # activation vectors per GEMV
     for gi, (label, fmt, N, K, xk) in enumerate(gemvs):
-        seed = synth.config_seed(1, gi) + 100 * rank
+        seed = WEIGHT_SEED + gi + 100 * rank
         W = synth.make_weights(fmt, N, K, seed)
         Wd = torch.from_numpy(W).to(dev)
         Ws.append([Wd] + [Wd.clone() for _ in range(copies - 1)])

@@ -146,23 +146,26 @@ def x_dtype_name(fmt) -> str:
 
 
 # Shapes of the benchmark configurations (name, fmt, N, K).
-CONFIGS = {
-    0: [("q4k_1024x1024", Q4_K, 1024, 1024)],
-    1: [("q4k_qkv_6144x4096", Q4_K, 6144, 4096),
-        ("q4k_gateup_28672x4096", Q4_K, 28672, 4096),
-        ("q4k_down_4096x14336", Q4_K, 4096, 14336)],
-    2: [("nvfp4_4096x14336", NVFP4, 4096, 14336),
-        ("nvfp4_14336x4096", NVFP4, 14336, 4096)],
-    3: [("tq1_0_4096x4096", TQ1_0, 4096, 4096),
-        ("tq1_0_11008x4096", TQ1_0, 11008, 4096)],
+# Shape sets of the measured workloads (one entry per GEMV: name, format, N, K), by name.
+SHAPE_SETS = {
+    "q4k_1024x1024": [("q4k_1024x1024", Q4_K, 1024, 1024)],
+    "q4k_llama8b_decode": [("q4k_qkv_6144x4096", Q4_K, 6144, 4096),
+                           ("q4k_gateup_28672x4096", Q4_K, 28672, 4096),
+                           ("q4k_down_4096x14336", Q4_K, 4096, 14336)],
+    "nvfp4_llama8b": [("nvfp4_4096x14336", NVFP4, 4096, 14336),
+                      ("nvfp4_14336x4096", NVFP4, 14336, 4096)],
+    "tq1_0": [("tq1_0_4096x4096", TQ1_0, 4096, 4096),
+              ("tq1_0_11008x4096", TQ1_0, 11008, 4096)],
 }
 # Decoder layer, hidden 4096, MLP 12288, 8 KV heads x 128.
 LAYER_SHAPES = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
                 ("gate", 12288, 4096), ("up", 12288, 4096), ("down", 4096, 12288)]
 LAYER_MIXED = {"q": Q4_K, "k": Q5_K, "v": Q6_K, "o": Q8_0, "gate": Q4_K, "up": Q4_K, "down": Q6_K}
-CONFIGS[4] = [(f"layer_{p}_{FORMAT_NAMES[LAYER_MIXED[p]]}_{n}x{k}", LAYER_MIXED[p], n, k)
-              for p, n, k in LAYER_SHAPES]
+SHAPE_SETS["layer"] = [(f"layer_{p}_{FORMAT_NAMES[LAYER_MIXED[p]]}_{n}x{k}", LAYER_MIXED[p], n, k)
+                       for p, n, k in LAYER_SHAPES]
 
 
-def config_seed(config_index: int, shape_index: int) -> int:
-    return 1000 * config_index + shape_index
+def shape_seed(set_name: str, shape_index: int) -> int:
+    """Seed of the synthetic weights of entry `shape_index` of a shape set: 1000 per set (in the
+    order above) plus the entry."""
+    return 1000 * list(SHAPE_SETS).index(set_name) + shape_index

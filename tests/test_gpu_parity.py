@@ -113,19 +113,19 @@ def test_ring_shapes_match_oracle(h, depth, rows):
         qgemv.set_option(h, qgemv.OPT_ROWS_PER_STAGE, 0)
 
 
-def _config_cases():
+def _shape_cases():
     out = []
-    for ci in (1, 2, 3, 4):
-        for si, (name, fmt, N, K) in enumerate(synth.CONFIGS[ci]):
-            out.append(pytest.param(ci, si, fmt, N, K, id=name))
+    for sname in ("q4k_llama8b_decode", "nvfp4_llama8b", "tq1_0", "layer"):
+        for si, (name, fmt, N, K) in enumerate(synth.SHAPE_SETS[sname]):
+            out.append(pytest.param(sname, si, fmt, N, K, id=name))
     return out
 
 
-@pytest.mark.parametrize("ci,si,fmt,N,K", _config_cases())
-def test_full_size_configs_on_sampled_rows(h, ci, si, fmt, N, K):
+@pytest.mark.parametrize("sname,si,fmt,N,K", _shape_cases())
+def test_full_size_workload_shapes_on_sampled_rows(h, sname, si, fmt, N, K):
     """Full sizes in the launch configuration the bench times (programmatic dependent
     launch on) and in the plain one, on sampled rows."""
-    seed = synth.config_seed(ci, si)
+    seed = synth.shape_seed(sname, si)
     W = synth.make_weights(fmt, N, K, seed)
     x = synth.make_x(fmt, K, seed)
     Wd, _ = dev_bytes(W)
@@ -139,7 +139,7 @@ def test_full_size_configs_on_sampled_rows(h, ci, si, fmt, N, K):
         finally:
             qgemv.set_option(h, qgemv.OPT_PDL, 0)
         assert qgemv.check_error(h) == qgemv.OK
-        assert_parity(y[rows], y_ref, S, f"config {ci} {N}x{K} pdl={pdl}")
+        assert_parity(y[rows], y_ref, S, f"{sname} {N}x{K} pdl={pdl}")
         assert np.all(np.isfinite(y))
 
 
@@ -176,9 +176,9 @@ def test_huge_row_counts_on_sampled_rows(h, fmt, N, K, mode):
     torch.cuda.empty_cache()
 
 
-def test_config0_full(h):
-    name, fmt, N, K = synth.CONFIGS[0][0]
-    _check_full(h, fmt, N, K, seed=synth.config_seed(0, 0), what=name)
+def test_q4k_1024x1024_full(h):
+    name, fmt, N, K = synth.SHAPE_SETS["q4k_1024x1024"][0]
+    _check_full(h, fmt, N, K, seed=synth.shape_seed("q4k_1024x1024", 0), what=name)
 
 
 @pytest.mark.parametrize("fmt", ALL)
