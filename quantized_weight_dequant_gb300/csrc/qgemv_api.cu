@@ -197,6 +197,9 @@ void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
 }
 
 int slice_of(int f) { return 8 * sb_bytes(f) + 8 * sb_bytes2(f); }
+// Decoder coefficient bytes per staged superblock (TQ1_0's collapse coefficients, prepared once
+// per CTA); must equal the decoder's kCoefSB.
+int coef_of(int f) { return f == F_TQ10 ? DecTQ10::kCoefSB : 0; }
 
 // Packed row bytes of stream 1 / 2, or false when the streaming kernel cannot take the
 // shape (rows must be whole superblocks and 16-byte multiples, at most 16 K-columns).
@@ -300,7 +303,7 @@ bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool gene
   };
   auto smem_of = [&](int d, int r) {
     size_t m = 0;
-    for (int i = 0; i < n; ++i) m = std::max(m, stream_smem(warps, d, r, slice_of(ps[i].f), Wk, red_rows[i], Kx).total);
+    for (int i = 0; i < n; ++i) m = std::max(m, stream_smem(warps, d, r, slice_of(ps[i].f), Wk, red_rows[i], Kx, coef_of(ps[i].f)).total);
     return m;
   };
   while (smem_of(D, R) > limit(D, R) && (D > 2 || R > Rmin)) {

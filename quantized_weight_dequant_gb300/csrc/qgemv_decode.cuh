@@ -65,6 +65,7 @@ struct XStage {
   uint16_t* q;
   float* e;
   int* s;
+  int* g;  // decoder coefficients (kCoefSB bytes per superblock), for decoders that have them
 };
 
 // d = c + a.h0 * b.b0 + a.h1 * b.b1 (lo) / a.h0 * b.b2 + a.h1 * b.b3 (hi); a two int16,
@@ -208,6 +209,7 @@ struct IntX {
 // 6-bit scale placed as an f16 subnormal gives d*s*2^-24 in one instruction.
 struct DecQ4K : IntX {
   static constexpr int kSB = 144, kSB2 = 0;
+  static constexpr int kCoefSB = 0;
   int c;
   uint32_t sel_s, sel_h, m1, m2, shm;
   uint32_t qoff;   // byte offset of this lane's quants in a block
@@ -288,6 +290,7 @@ struct DecQ4K : IntX {
 // brings it to bit 4 of each byte, next to its nibble, before the dot product.
 struct DecQ5K : DecQ4K {
   static constexpr int kSB = 176, kSB2 = 0;
+  static constexpr int kCoefSB = 0;
   uint32_t rl, rh;  // rotate amounts bringing bit 2c / 2c+1 of each byte to bit 4
 
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
@@ -340,6 +343,7 @@ struct DecQ5K : DecQ4K {
 // aligned), so quant words are read as 16-bit pairs.
 struct DecQ6K : IntX {
   static constexpr int kSB = 210, kSB2 = 0;
+  static constexpr int kCoefSB = 0;
   int c;
   uint32_t rlo, rhi;  // rotate amounts bringing qh bits 2rr / 2rr+4 of each byte to bit 4
 
@@ -398,6 +402,7 @@ struct DecQ6K : IntX {
 // 64c + 32e + j).  The int8 codes are dotted directly with signed dp2a.
 struct DecQ80 : IntX {
   static constexpr int kSB = 272, kSB2 = 0;
+  static constexpr int kCoefSB = 0;
   int c;
 
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
@@ -445,6 +450,7 @@ struct DecQ80 : IntX {
 // than the largest lose low bits); the power of two is removed per chunk from the result.
 struct DecNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
+  static constexpr int kCoefSB = 0;
   uint32_t xr[32];
   float xf0, xf1;
   int c;
@@ -580,38 +586,77 @@ struct DecTQ10 {
     if ((i & 31) == 0) X.e[i >> 5] = p2(-e);
   }
   __device__ __forceinline__ void init(int c_) { c = c_; }
-  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
-    const uint32_t qa = static_cast<uint32_t>(__cvta_generic_to_shared(X.q)) + 512u * sbcol;
-    auto xi = [&](int p, int n) -> int {
-      return active ? static_cast<int>(static_cast<int16_t>(lds_u16(qa + 2 * elem_of(p, n)))) : 0;
-    };
-    xsum = 0;
+  // Collapse coefficients of every lane piece of the staged x, computed once per CTA by all
+  // its threads (every warp of the CTA reads the same pieces).  Item (superblock, piece c,
+  // part): parts 0..2 are the piece's qs words, part 3 its qh byte; each writes its g_k and
+  // its partial sum of x into the piece's 40 words: g of word w at 10 w + 2 (k - 1) + h (h: bytes
+  // 0,1 / 2,3 as int16 pairs), the qh g_k at 30 + k - 1, the four partial sums at 34..37.
+  static constexpr int kCoefSB = 4 * 160;
+  __device__ static void prep(const XStage& X, int nsb, int tid, int nthreads) {
+    const uint32_t q0 = static_cast<uint32_t>(__cvta_generic_to_shared(X.q));
+    for (int it = tid; it < 16 * nsb; it += nthreads) {
+      const int sb = it >> 4, c = (it >> 2) & 3, part = it & 3;
+      const uint32_t qa = q0 + 512u * sb;
+      auto xi = [&](int p, int n) -> int { return static_cast<int>(static_cast<int16_t>(lds_u16(qa + 2 * elem_of(p, n)))); };
+      int* g = X.g + (4 * sb + c) * 40;
+      int xs = 0;
+      if (part < 3) {
+        int gg[4][5];
 #pragma unroll
-    for (int w = 0; w < 3; ++w) {
-      int g[4][5];
+        for (int j = 0; j < 4; ++j) {
+          const int p = 12 * c + 4 * part + j;
+          int y[6];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = 12 * c_ + 4 * w + j;
-        int y[6];
+          for (int n = 0; n < 5; ++n) y[n] = xi(p, n), xs += y[n];
+          y[5] = 0;
 #pragma unroll
-        for (int n = 0; n < 5; ++n) y[n] = xi(p, n), xsum += y[n];
-        y[5] = 0;
+          for (int k = 1; k <= 5; ++k) gg[j][k - 1] = y[k - 1] - 3 * y[k];
+        }
 #pragma unroll
-        for (int k = 1; k <= 5; ++k) g[j][k - 1] = y[k - 1] - 3 * y[k];
+        for (int k = 0; k < 5; ++k) {
+          g[10 * part + 2 * k] = static_cast<int>((static_cast<uint32_t>(gg[0][k]) & 0xFFFFu) |
+                                                  (static_cast<uint32_t>(gg[1][k]) << 16));
+          g[10 * part + 2 * k + 1] = static_cast<int>((static_cast<uint32_t>(gg[2][k]) & 0xFFFFu) |
+                                                      (static_cast<uint32_t>(gg[3][k]) << 16));
+        }
+      } else {
+        int y[5];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) y[n] = xi(48 + c, n), xs += y[n];
+        y[4] = 0;
+#pragma unroll
+        for (int k = 1; k <= 4; ++k) g[30 + k - 1] = y[k - 1] - 3 * y[k];
       }
-#pragma unroll
-      for (int k = 0; k < 5; ++k) {
-        gw[w][k][0] = (static_cast<uint32_t>(g[0][k]) & 0xFFFFu) | (static_cast<uint32_t>(g[1][k]) << 16);
-        gw[w][k][1] = (static_cast<uint32_t>(g[2][k]) & 0xFFFFu) | (static_cast<uint32_t>(g[3][k]) << 16);
-      }
+      g[34 + part] = xs;
     }
-    int y[5];
+  }
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
+    if (active) {
+      const uint32_t ga = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + 160u * (4 * sbcol + c_);
+      uint32_t v[40];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) y[n] = xi(48 + c_, n), xsum += y[n];
-    y[4] = 0;
+      for (int i = 0; i < 10; ++i) {
+        const uint4 t = lds_v4(ga + 16 * i);
+        v[4 * i] = t.x, v[4 * i + 1] = t.y, v[4 * i + 2] = t.z, v[4 * i + 3] = t.w;
+      }
 #pragma unroll
-    for (int k = 1; k <= 4; ++k) gq[k - 1] = y[k - 1] - 3 * y[k];
-    xf = active ? X.e[sbcol] : 0.f;
+      for (int w = 0; w < 3; ++w)
+#pragma unroll
+        for (int k = 0; k < 5; ++k) gw[w][k][0] = v[10 * w + 2 * k], gw[w][k][1] = v[10 * w + 2 * k + 1];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) gq[k] = static_cast<int>(v[30 + k]);
+      xsum = static_cast<int>(v[34]) + static_cast<int>(v[35]) + static_cast<int>(v[36]) + static_cast<int>(v[37]);
+      xf = X.e[sbcol];
+    } else {
+#pragma unroll
+      for (int w = 0; w < 3; ++w)
+#pragma unroll
+        for (int k = 0; k < 5; ++k) gw[w][k][0] = gw[w][k][1] = 0u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) gq[k] = 0;
+      xsum = 0;
+      xf = 0.f;
+    }
   }
 
   struct Raw {

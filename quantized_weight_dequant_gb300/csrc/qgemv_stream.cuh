@@ -111,18 +111,21 @@ __host__ __device__ constexpr int slice_bytes() {
 }
 
 // Shared memory: [rings: warps * D * R * slice][reduction buffer][x staging: q (2K bytes),
-// e (K/32 floats), s (K/16 ints)][never-completing barrier], each part 16-byte aligned.
+// e (K/32 floats), s (K/16 ints)][decoder coefficients: coef_sb bytes per superblock of the
+// staged x][never-completing barrier], each part 16-byte aligned.
 struct StreamSmem {
-  size_t red, xq, xe, xs, bar, total;
+  size_t red, xq, xe, xs, xc, bar, total;
 };
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
-__host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int slice, int Wk, int red_rows, int K) {
+__host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int slice, int Wk, int red_rows, int K,
+                                                  int coef_sb) {
   StreamSmem m;
   m.red = static_cast<size_t>(warps) * D * R * slice;
   m.xq = align16(m.red + (Wk > 1 ? static_cast<size_t>(red_rows) * Wk * 4 : 0));
   m.xe = align16(m.xq + static_cast<size_t>(K) * 2);
   m.xs = align16(m.xe + static_cast<size_t>(K / 32) * 4);
-  m.bar = align16(m.xs + static_cast<size_t>(K / 16) * 4);
+  m.xc = align16(m.xs + static_cast<size_t>(K / 16) * 4);
+  m.bar = align16(m.xc + static_cast<size_t>(K / 256) * coef_sb);
   m.total = m.bar + 16;
   return m;
 }
@@ -213,11 +216,11 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
 
   // The staging buffer holds the K-columns this CTA reads: all of x (fused) or one column.
   const int Kx = a.split ? min(2048, 256 * a.nsb) : 256 * a.nsb;
-  const StreamSmem L = stream_smem(nwarps, D, R, SLICE, a.Wk, a.red_rows, Kx);
+  const StreamSmem L = stream_smem(nwarps, D, R, SLICE, a.Wk, a.red_rows, Kx, Dec::kCoefSB);
   uint8_t* ring = smem + static_cast<size_t>(warp) * D * STAGE;
   float* red = reinterpret_cast<float*>(smem + L.red);
   const XStage X{reinterpret_cast<uint16_t*>(smem + L.xq), reinterpret_cast<float*>(smem + L.xe),
-                 reinterpret_cast<int*>(smem + L.xs)};
+                 reinterpret_cast<int*>(smem + L.xs), reinterpret_cast<int*>(smem + L.xc)};
   uint64_t* never_bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
   pdl_launch_dependents();  // the next kernel may start copying its weights right away
@@ -357,6 +360,10 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   }
   __syncthreads();
   QG_TRACE(2);
+  if constexpr (Dec::kCoefSB > 0) {  // per-CTA decoder coefficients of the staged x
+    Dec::prep(X, (pc1 - pc0) / 32, threadIdx.x, blockDim.x);
+    __syncthreads();
+  }
   Dec dec;
   dec.init(lane & 3);
   dec.load_x(X, 8 * (wk - kc0) + col, lane & 3, active);  // superblock index within the buffer
