@@ -53,9 +53,11 @@ def _check(Y, X, fmt, W, N, K, ms, what):
 # (N, K, M): one K-block; ragged N and M; 129 rows (a 256-row tile, mostly outside X); long K
 # at M = 64 (64-row tiles, 128-wide stages, 8 K splits); K-blocks not a multiple of the ring
 # depth (128- and 64-wide stages); a full prefill shape (2 splits); tiles enough for every SM
-# (no split)
+# (no split); one 64-wide K-block on 256-row tiles; 4096 rows of X with one K-block; 65 rows
+# (the first 128-row tile)
 TC_CASES = [(128, 128, 9), (200, 4096, 300), (1000, 2048, 129), (256, 14336, 64), (333, 1152, 77),
-            (200, 960, 150), (4096, 4096, 512), (130, 1024, 1000), (4096, 1024, 1100)]
+            (200, 960, 150), (4096, 4096, 512), (130, 1024, 1000), (4096, 1024, 1100),
+            (384, 64, 300), (128, 128, 4096), (520, 2048, 65)]
 
 
 @pytest.mark.parametrize("N,K,M", TC_CASES)
