@@ -397,9 +397,9 @@ __device__ __forceinline__ void lds_run(uint32_t addr, uint32_t (&w)[N]) {
 // boundaries, so a stage copies the aligned 16-byte chunks that cover its superblocks (the
 // stage's data starts kMaxOff or fewer bytes into the slot) and reads words with lds_run.
 //
-// TQ1_0 ("ternary packing" page, the il walk): byte m of qs[0..32) holds digit n of elements
-// 32 n + m, byte 32 + m of qs holds digit n of elements 160 + 16 n + m, byte m of qh holds digit
-// n < 4 of elements 240 + 4 n + m.  Lane t4 takes qs bytes [8 t4, 8 t4 + 8) (steps 2 n + w for
+// TQ1_0 ("metal: TQ1_0 kernel performance", section 2, the il walk): byte m of qs[0..32)
+// holds digit n of elements 32 n + m, byte 32 + m of qs holds digit n of elements 160 + 16 n +
+// m, byte m of qh holds digit n < 4 of elements 240 + 4 n + m.  Lane t4 takes qs bytes [8 t4, 8 t4 + 8) (steps 2 n + w for
 // its words w = 0, 1), qs bytes [32 + 4 t4, 36 + 4 t4) (steps 10 + n) and digit n = t4 of the
 // qh word (step 15).  The digits come out of the floor pair as in the stream decoder: with the
 // even and the odd bytes in 16-bit lanes, q <- 3 q splits into the digit (bits 8..9) and the
