@@ -121,6 +121,21 @@ def test_batch_automatic_path_choice(h, fmt, N, M):
     _check(Y, X, fmt, W, N, K, what=f"auto {synth.FORMAT_NAMES[fmt]} {N}x{K} M={M}")
 
 
+def test_batch_q6k_full_range_scales(h):
+    """Q6_K scales over the whole int8 range: (q6 - 32) sc then exceeds 2048 in magnitude and
+    is rounded once to fp16 in the batch kernel (relative error <= 2^-11 per weight), still
+    within the GEMV bound against the oracle's exact weights."""
+    fmt, N, K = synth.Q6_K, 96, 4096
+    W = synth.make_weights(fmt, N, K, seed=13).copy()
+    blocks = W.reshape(-1, 210)
+    rng = np.random.default_rng(13)
+    blocks[:, 192:208] = rng.integers(-128, 128, size=(blocks.shape[0], 16)).astype(np.int8).view(np.uint8)
+    Wd, _ = dev_bytes(W)
+    X = _xs(fmt, 8, K, seed=13)
+    Y = _run(h, fmt, X, Wd, N, K)
+    _check(Y, X, fmt, W, N, K, what="Q6_K full-range scales")
+
+
 def test_batch_nvfp4_wide_range_vectors(h):
     """Vectors whose magnitudes differ by 2^40 get their own fp16 exponent window."""
     fmt, N, K = synth.NVFP4, 64, 4096
