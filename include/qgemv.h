@@ -258,7 +258,9 @@ qgemv_status_t qgemv_run_ex(qgemv_handle_t h, qgemv_format_t fmt, const void* x,
  * single-vector launches are faster), with rows whose packed length is a multiple of 16 bytes
  * (K a multiple of 2048 for TQ1_0 and Q6_K, of 256 for the others) and M * N * ceil(K / 1024)
  * within the handle's workspace (4 Mi column sums); other calls run the single-vector path
- * once per vector. */
+ * once per vector.  Input domain of the tensor-core path: a Q8_0 weight d q is formed in
+ * fp16, so weights must be below 65504 in magnitude (quantised model weights are many orders
+ * of magnitude smaller); the single-vector path has no such limit. */
 #define QGEMV_MAX_BATCH 8
 
 /* x: device, M rows of K 16-bit values (fp16; bf16 for NVFP4), row-major, 16-byte aligned.
