@@ -1,6 +1,7 @@
 // qgemv_run_noalloc: the split-K streaming GEMV for callers that cannot allocate device
-// memory, with its scratch (column sums, per-range counters, error word) in fixed
-// file-scope device arrays instead of a handle's workspace.  See include/qgemv.h.
+// memory, with its scratch (column sums and per-range counters) in fixed file-scope device
+// arrays instead of a handle's workspace.  See include/qgemv.h.  No error word: the kernel
+// writes one only for the stall test hook, which this entry point never sets.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,7 +31,6 @@ constexpr int kMaxWarps = 16;
 // exits; every call on a device shares them.
 static __device__ __align__(256) float g_noalloc_ws[QGEMV_NOALLOC_MAX_COLUMN_SUMS];
 static __device__ __align__(256) int g_noalloc_cnt[kMaxRanges];
-static __device__ __align__(256) int g_noalloc_err[4];
 
 struct DeviceSetup {
   bool ready = false;
@@ -38,7 +38,6 @@ struct DeviceSetup {
   size_t dyn_smem_max[6][3][3] = {};  // [format][R 1/2/4][D 2/3/4]
   float* ws = nullptr;                 // device addresses of the arrays above
   int* cnt = nullptr;
-  int* err = nullptr;
 };
 
 std::mutex g_setup_mu;
@@ -78,8 +77,7 @@ qgemv_status_t setup(int dev, DeviceSetup** out) {
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return QGEMV_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return QGEMV_ERR_NO_DEVICE;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.ws), g_noalloc_ws) != cudaSuccess ||
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&s.cnt), g_noalloc_cnt) != cudaSuccess ||
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_noalloc_err) != cudaSuccess) {
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&s.cnt), g_noalloc_cnt) != cudaSuccess) {
       cudaGetLastError();
       return QGEMV_ERR_CUDA;
     }
@@ -172,7 +170,7 @@ extern "C" qgemv_status_t qgemv_run_noalloc(qgemv_format_t fmt, const void* x, c
   a.Wk = Wk;
   a.P = P;
   a.red_rows = 0;
-  a.err = s->err;
+  a.err = nullptr;  // written only under the stall test hook (test_stall = 0 here)
   a.spin_ns = 1000000000ull;
   a.test_stall = 0;
   a.pdl = 0;

@@ -1,5 +1,5 @@
-// Thin inline-PTX wrappers used by the qgemv kernels (sm_103a): shared-memory mbarriers,
-// 1-D bulk global->shared copies, proxy fences, named barriers and the global timer.
+// Thin inline-PTX wrappers used by the qgemv kernels (sm_103a): shared-memory loads,
+// mbarriers, programmatic dependent launch and a warp sum.
 #pragma once
 #include <cstdint>
 
@@ -54,32 +54,9 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Orders this thread's earlier generic-proxy shared accesses before later async-proxy ones.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16) from global `src` (16-byte aligned) to shared `dst`
-// (16-byte aligned); completion is signalled on mbarrier `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// L2 policy for data read exactly once (the packed weights).
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -113,12 +90,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Waits for phase `parity` of `bar` to complete, giving up once about `limit_ns` have
 // passed after the first unsuccessful probe (measured in SM cycles, counted as 4 per ns so
 // the bound holds at any clock up to 4 GHz).  The waiting thread sleeps in the probe.
@@ -134,10 +105,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -147,12 +114,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// Exact power of two 2^e as float, e in [-126, 127].
-__host__ __device__ constexpr float pow2f(int e) {
-  return e >= 0 ? float(1ull << (e > 62 ? 62 : e)) * (e > 62 ? pow2f(e - 62) : 1.0f)
-                : 1.0f / pow2f(-e);
 }
 
 }  // namespace qg

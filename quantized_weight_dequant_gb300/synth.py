@@ -14,7 +14,7 @@ Block layouts (byte offsets inside one block, little-endian fp16):
 * Q6_K  (256 weights, 210 B): ql[128] @0, qh[64] @128, int8 scales[16] @192, d @208.
 * Q8_0  (32 weights, 34 B):   d @0, int8 qs[32] @2.
   (Q5_K, Q6_K and Q8_0 are only named on the Metal GEMV page, section "UD-Q4_K_XL";
-  their layouts are the standard ggml ones, a reading recorded in the design doc.)
+  their layouts are taken to be the standard ggml ones: a reading, not on the pages.)
 * TQ1_0 (256 weights, 54 B):  qs[48] @0 (5 base-3 digits per byte), qh[4] @48
   (4 digits per byte), d fp16 @52.  ("metal: TQ1_0 kernel performance", section 1.)
 * NVFP4 W4A16 (Mojo ``fp4_gemv`` page): E2M1 nibbles [N, K/2] (low nibble = even

@@ -1,6 +1,7 @@
 """GPU parity of qgemv_run_gemm, the product for any number M of activation rows.  NVFP4 with
 M > 8 runs the tcgen05 tensor-core kernel (tiles of 128 weight rows x 256 or 128 rows of X, X
-by TMA, the weights dequantised to bf16 in shared memory, fp32 accumulation in TMEM); the other
+by TMA, the weights dequantised to bf16 into tensor memory as the A operand, fp32 accumulation
+in TMEM); the other
 formats and shapes go through the batch path in chunks of 8.  Every checked output row meets
 |y - y_ref| <= 2e-3 * sum|x w| + 1e-5 against the oracle's GEMV of its own activation row;
 large cases check sampled rows of X (always the first, middle and last)."""

@@ -2,16 +2,19 @@
 memory (a host application that owns all device memory, a capped or instrumented
 allocator, a latency-critical path that cannot afford an allocation's synchronisation).
 It keeps its scratch in fixed arrays inside the library, so these checks call it through
-the C-ABI twice in a row, on the same and on different shapes, and compare each result with
-qgemv_run's on the same inputs, within the GEMV tolerance used by every parity test
-(|y - y_ref| <= 2e-3 * sum|x w| + 1e-5, with sum|x w| from the oracle).  The file is named
-to be collected last; it also passes on its own in a fresh process."""
+the C-ABI twice in a row and compare every result with the CPU oracle on the same inputs,
+within the GEMV tolerance of every parity test (|y - y_ref| <= 2e-3 * sum|x w| + 1e-5),
+and with qgemv_run's result within the same tolerance; two calls in a row give the same
+bits.  Covered: the shapes at
+the scratch limit exactly (N * ceil(K / 2048) equal to its capacity) and at the longest K
+(16 K-columns), and a call on a side stream.  The file is named to be collected last; it
+also passes on its own in a fresh process."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import ATOL, RTOL, dev_bytes, dev_x
+from gpu_util import assert_parity, dev_bytes, dev_x, sample_rows
 from quantized_weight_dequant_gb300 import qgemv, synth
 
 pytestmark = pytest.mark.gpu
@@ -28,40 +31,62 @@ def h():
     handle.close()
 
 
-def _inputs(fmt, N, K, seed):
+CASES = [(synth.Q4_K, 4096, 14336), (synth.NVFP4, 700, 14336), (synth.Q4_K, 2000, 4096),
+         (synth.Q6_K, 129, 12288), (synth.Q8_0, 300, 6144), (synth.TQ1_0, 77, 4096),
+         (synth.Q5_K, 50, 2048), (synth.Q4_K, 40, 32768)]
+
+
+def _two_calls(h, fmt, N, K, seed, rows=None, stream=None):
     W = synth.make_weights(fmt, N, K, seed)
     x = synth.make_x(fmt, K, seed)
     Wd, _ = dev_bytes(W)
-    _, S = oracle.gemv(fmt, x, W, N, K)
-    return Wd, dev_x(x), S
-
-
-def _close(a, b, S):
-    err = np.abs(a.astype(np.float64) - b.astype(np.float64))
-    bad = np.nonzero(~(err <= RTOL * S + ATOL))[0]
-    assert bad.size == 0, (bad[:5], err[bad[:5]])
-
-
-CASES = [(synth.Q4_K, 4096, 14336), (synth.NVFP4, 700, 14336), (synth.Q4_K, 2000, 4096),
-         (synth.Q6_K, 129, 12288), (synth.Q8_0, 300, 6144), (synth.TQ1_0, 77, 4096),
-         (synth.Q5_K, 50, 2048)]
-
-
-def test_noalloc_matches_run_on_two_calls_in_a_row(h):
+    xd = dev_x(x)
+    if rows is None:
+        y_ref, S = oracle.gemv(fmt, x, W, N, K)
+        rows = np.arange(N)
+    else:
+        y_ref, S = oracle.gemv_rows(fmt, x, W, N, K, rows)
+    y_run = torch.empty(N, dtype=torch.float32, device="cuda")
+    qgemv.run(h, fmt, xd, Wd, N, K, y_run)
+    torch.cuda.synchronize()
     prev = None
-    for fmt, N, K in CASES:
-        Wd, xd, S = _inputs(fmt, N, K, seed=N + K + fmt)
-        y_ref = torch.empty(N, dtype=torch.float32, device="cuda")
-        qgemv.run(h, fmt, xd, Wd, N, K, y_ref)
-        for call in range(2):  # the second call finds the scratch as the first left it
-            y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    for call in range(2):  # the second call finds the scratch as the first left it
+        y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+        if stream is None:
             qgemv.run_noalloc(fmt, xd, Wd, N, K, y)
-            torch.cuda.synchronize()
-            _close(y.cpu().numpy(), y_ref.cpu().numpy(), S)
-            if call == 1:
-                assert torch.equal(y, prev), "results differ between two calls in a row"
-            prev = y.clone()
-    assert qgemv.check_error(h) == qgemv.OK
+        else:
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                qgemv.run_noalloc(fmt, xd, Wd, N, K, y, stream=stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        yh = y.cpu().numpy()
+        assert_parity(yh[rows], y_ref, S, f"noalloc {synth.FORMAT_NAMES[fmt]} {N}x{K} call {call}")
+        # against the existing entry point, within the same tolerance (their launch plans can
+        # differ, e.g. fused K-columns in qgemv_run, so the bits may too)
+        assert_parity(yh[rows], y_run.cpu().numpy()[rows].astype(np.float64), S,
+                      f"noalloc against qgemv_run {synth.FORMAT_NAMES[fmt]} {N}x{K} call {call}")
+        if prev is not None:
+            assert torch.equal(y, prev), "results differ between two calls in a row"
+        prev = y.clone()
+
+
+@pytest.mark.parametrize("fmt,N,K", CASES)
+def test_noalloc_matches_oracle_on_two_calls_in_a_row(h, fmt, N, K):
+    _two_calls(h, fmt, N, K, seed=N + K + fmt)
+
+
+def test_noalloc_at_the_scratch_limit_exactly(h):
+    """N * ceil(K / 2048) = 16384 * 16 = the scratch capacity: accepted, and correct on sampled
+    rows (the last row range ends at the last column sum of the scratch)."""
+    N, K = qgemv.NOALLOC_MAX_COLUMN_SUMS // 16, 32768
+    assert N * (K // 2048) == qgemv.NOALLOC_MAX_COLUMN_SUMS
+    _two_calls(h, synth.Q4_K, N, K, seed=5, rows=sample_rows(N, 96, seed=5))
+    torch.cuda.empty_cache()
+
+
+def test_noalloc_on_a_side_stream(h):
+    _two_calls(h, synth.Q4_K, 1000, 14336, seed=8, stream=torch.cuda.Stream())
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(h):
@@ -72,5 +97,8 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(h):
     st = qgemv.run_noalloc(synth.Q4_K, x, W, N, K, y, check=False)
     assert st == qgemv.ERR_TOO_LARGE
     assert "scratch" in qgemv.status_string(st)
+    N2 = qgemv.NOALLOC_MAX_COLUMN_SUMS // 16 + 1  # one row past the limit at 16 K-columns
+    assert qgemv.run_noalloc(synth.Q4_K, torch.zeros(32768, dtype=torch.int16, device="cuda"), W, N2, 32768, y,
+                             check=False) == qgemv.ERR_TOO_LARGE
     assert qgemv.run_noalloc(synth.Q4_K, x, W, 5, 1000, y, check=False) == qgemv.ERR_BAD_SHAPE
     torch.cuda.synchronize()
