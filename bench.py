@@ -108,6 +108,38 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_traffic(build_marker: str, kernel: str):
+    """ncu DRAM bytes per launch of `kernel` recorded in profiles/roofline_traffic.json for
+    this build (the library's source digest); None when the record is for another build."""
+    p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("build") != build_marker.split(":", 1)[-1]:
+        return None, f"recorded for build {rec.get('build')}, not this one"
+    k = rec.get("kernels", {}).get(kernel)
+    if not k:
+        return None, None
+    return float(k["dram_bytes_per_launch"]), rec.get("command")
+
+
+# The benchmark configurations at M = 1, each GEMV timed on its own: (config, [(label, fmt,
+# N, K)]).  Config 4 is the Qwen-like layer, in the mixed assignment and in every
+# projection x format pair.
+CONFIGS = [
+    ("config0_q4k_1024x1024", [("w", synth.Q4_K, 1024, 1024)]),
+    ("config1_q4k_llama8b_decode", [("qkv", synth.Q4_K, 6144, 4096), ("gate_up", synth.Q4_K, 28672, 4096),
+                                    ("down", synth.Q4_K, 4096, 14336)]),
+    ("config2_nvfp4_llama8b", [("4096x14336", synth.NVFP4, 4096, 14336), ("14336x4096", synth.NVFP4, 14336, 4096)]),
+    ("config3_tq1_0", [("4096x4096", synth.TQ1_0, 4096, 4096), ("11008x4096", synth.TQ1_0, 11008, 4096)]),
+    ("config4_layer_mixed", [(p, synth.LAYER_MIXED[p], n, k) for p, n, k in synth.LAYER_SHAPES]),
+    ("config4_layer_every_projection_x_format",
+     [(f"{p}:{synth.FORMAT_NAMES[f]}", f, n, k) for p, n, k in synth.LAYER_SHAPES
+      for f in (synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.Q8_0)]),
+]
+
+
 # ------------------------------------------------------------------ clocks sampler
 class Clocks:
     FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
@@ -413,6 +445,116 @@ def run_profile_prefill(args, gemvs):
     return 0
 
 
+def graph_us(launch, copies: int, stream, R: int = 200, reps: int = 7) -> float:
+    """Mean µs per launch: a CUDA graph of R launches cycling over `copies` weight copies,
+    replayed `reps` times after one warm replay; median over the replays (CUDA events on the
+    launch stream)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(R):
+            launch(i % copies)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    samples = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        stream.synchronize()
+        samples.append(a.elapsed_time(b) * 1e3 / R)
+    del g
+    return statistics.median(samples)
+
+
+def flushed_single_us(launch, stream, l2: int, reps: int = 15) -> float:
+    """Median µs of one launch with L2 flushed just before it: a buffer of twice the L2 size
+    is written, then the launch alone is bracketed by CUDA events on its stream."""
+    import torch
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=stream.device)
+    samples = []
+    for i in range(reps + 2):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(0)
+            b.record(stream)
+        stream.synchronize()
+        if i >= 2:
+            samples.append(a.elapsed_time(b) * 1e3)
+    del flush
+    return statistics.median(samples)
+
+
+def run_configs(h, dev, stream, l2: int, pdl: int, peak: float):
+    """Every GEMV of the benchmark configurations, one at a time: µs per call in the graph
+    protocol (programmatic dependent launch as set), GB/s and fraction of the HBM peak, and
+    the single-launch latency with L2 flushed (no dependent launch).  Config 4's mixed layer
+    is also timed as a step of its 7 GEMVs.  Returns {config: {...}} and the launch count."""
+    import torch
+
+    from quantized_weight_dequant_gb300 import qgemv
+
+    done, out, launches = {}, {}, 0
+    for cname, gl in CONFIGS:
+        rows = {}
+        for label, fmt, N, K in gl:
+            key = (fmt, N, K)
+            if key not in done:
+                W = torch.from_numpy(synth.make_weights(fmt, N, K, WEIGHT_SEED + N + K + fmt)).to(dev)
+                copies = max(2, math.ceil(3 * l2 / W.numel()))
+                Ws = [W] + [W.clone() for _ in range(copies - 1)]
+                x = torch.from_numpy(synth.make_x(fmt, K, WEIGHT_SEED).view(np.int16).copy()).to(dev)
+                y = torch.empty(N, dtype=torch.float32, device=dev)
+
+                def launch(c, Ws=Ws, x=x, y=y, fmt=fmt, N=N, K=K):
+                    qgemv.run(h, fmt, x, Ws[c], N, K, y, stream=stream)
+
+                us = graph_us(launch, copies, stream)
+                qgemv.set_option(h, qgemv.OPT_PDL, 0)
+                us1 = flushed_single_us(launch, stream, l2)
+                qgemv.set_option(h, qgemv.OPT_PDL, pdl)
+                st = qgemv.check_error(h, stream)
+                if st != qgemv.OK:
+                    raise RuntimeError(f"qgemv error {qgemv.status_string(st)} on {key}")
+                b = gemv_bytes(fmt, N, K)
+                done[key] = {"shape": f"{synth.FORMAT_NAMES[fmt]} {N}x{K}", "us": round(us, 3),
+                             "GB/s": round(b / (us * 1e-6) / 1e9, 1), "frac": round(b / (us * 1e-6) / 1e9 / peak, 4),
+                             "us_single_l2_flushed": round(us1, 3), "MB": round(b / 1e6, 3)}
+                launches += 200 * 8 + 17
+                del Ws, W, x, y
+            rows[label] = done[key]
+        out[cname] = {"gemvs": rows}
+    # the mixed layer as one step: 7 launches in order, x of the layer shared, down on its own x
+    gl = dict(CONFIGS)["config4_layer_mixed"]
+    Wl, xs, ys = [], {}, []
+    step_w = sum(synth.packed_bytes(f, n, k) for _, f, n, k in gl)
+    copies = max(2, math.ceil(3 * l2 / step_w))
+    for i, (label, fmt, N, K) in enumerate(gl):
+        W = torch.from_numpy(synth.make_weights(fmt, N, K, WEIGHT_SEED + i)).to(dev)
+        Wl.append([W] + [W.clone() for _ in range(copies - 1)])
+        xs.setdefault(K, torch.from_numpy(synth.make_x(fmt, K, WEIGHT_SEED + K).view(np.int16).copy()).to(dev))
+        ys.append(torch.empty(N, dtype=torch.float32, device=dev))
+
+    def step(c):
+        for i, (label, fmt, N, K) in enumerate(gl):
+            qgemv.run(h, fmt, xs[K], Wl[i][c], N, K, ys[i], stream=stream)
+
+    us = graph_us(step, copies, stream, R=50)
+    sb = sum(gemv_bytes(f, n, k) for _, f, n, k in gl)
+    out["config4_layer_mixed"]["step"] = {"launches": len(gl), "us": round(us, 3),
+                                          "GB/s": round(sb / (us * 1e-6) / 1e9, 1),
+                                          "frac": round(sb / (us * 1e-6) / 1e9 / peak, 4)}
+    launches += 50 * 8 * len(gl)
+    del Wl, xs, ys
+    torch.cuda.empty_cache()
+    return out, launches
+
+
 def run_ours(args, gemvs, rank, world):
     import torch
 
@@ -605,8 +747,15 @@ def run_ours(args, gemvs, rank, world):
     dom = max(units, key=lambda u_: unit_bytes(gemvs, u_[1], u_[2], B))[0]
     peak, peak_kind = load_peaks()
     achieved = per_call[dom]["GB/s"]
+    dom_idx = [u_ for u_ in units if u_[0] == dom][0][1]
+    tkey = ("+".join(f"{synth.FORMAT_NAMES[gemvs[i][1]]}_{gemvs[i][2]}x{gemvs[i][3]}" for i in dom_idx)
+            + ("_group" if dom in grouped else "") + (f"_batch{B}" if B > 1 else ""))
+    traffic, traffic_cmd = load_traffic(qgemv.build_marker(), tkey)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": args.traffic,
+                "traffic": traffic,
+                "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one {tkey} launch of this "
+                                   f"build (profiles/roofline_traffic.json): {traffic_cmd}") if traffic is not None
+                else (traffic_cmd or f"no ncu record of {tkey} for this build"),
                 "kernel": f"{'group_kernel' if dom in grouped else 'batch_kernel' if B > 1 else 'stream_kernel'} "
                           f"{per_call[dom]['shape']}" + (f" x {B} vectors" if B > 1 else ""),
                 "peak_kind": f"hbm_gbs of {peak_kind} (copy bandwidth)",
@@ -666,7 +815,15 @@ def run_ours(args, gemvs, rank, world):
                   + ": per step one pinned H2D copy of the step's packed x, one qgemv_run / qgemv_run_group / "
                   "qgemv_run_batch per launch unit, one D2H copy of the packed outputs; weights resident"}
 
-    cpu = None
+    configs = None
+    if rank == 0 and not args.no_configs and B == 1:
+        configs, _ = run_configs(h, dev, stream, l2, args.pdl, peak)
+        configs["how"] = ("each GEMV alone: µs per call = a CUDA graph of 200 launches over rotating weight copies "
+                          "(> 3x L2), programmatic dependent launch %s, CUDA events; us_single_l2_flushed = one "
+                          "launch after writing a buffer of twice the L2 size, no dependent launch, median of 15; "
+                          "frac against hbm_gbs of MEASURED_PEAKS.json" % ("on" if args.pdl else "off"))
+
+    cpu = cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         sampler = OracleSampler(gemvs, threads, batch=B)
@@ -678,6 +835,15 @@ def run_ours(args, gemvs, rank, world):
         sampler.close()
         cpu = {"value": statistics.median(rates), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{sample}; median of {len(rates)} samples, {spent:.1f} s wall in total"}
+        sampler1 = OracleSampler(gemvs, 1, batch=B)  # the same oracle on one thread
+        rates1, spent1 = [], 0.0
+        while spent1 < args.cpu_seconds / 2 or len(rates1) < 3:
+            rate, dt, sample1 = sampler1.run(max(0.3, args.cpu_seconds / 10))
+            rates1.append(rate)
+            spent1 += dt
+        sampler1.close()
+        cpu1 = {"value": statistics.median(rates1), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{sample1}; median of {len(rates1)} samples, {spent1:.1f} s wall in total"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -693,7 +859,8 @@ def run_ours(args, gemvs, rank, world):
                            "launches": [f"{u_[0]}:{'+'.join(gemvs[i][0] for i in u_[1])}"
                                         + (":swiglu" if u_[2] else "") for u_ in units],
                            "pdl": bool(args.pdl)},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu, "cpu_baseline_1_thread": cpu1, "e2e": e2e,
+                "configs": configs,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "us_per_call": per_call, "impl": "ours", "build": qgemv.build_marker(),
                 "gpu": props.name}
@@ -725,8 +892,8 @@ def main(argv=None):
                     help="also time each GEMV with dense bf16 weights through cuBLAS (context only)")
     ap.add_argument("--prefill", type=int, default=0,
                     help="M > 0: time the NVFP4 GEMM of M activation rows (the prefill path) instead of the GEMV")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant kernel, when known for this build")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing every GEMV of the five benchmark configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

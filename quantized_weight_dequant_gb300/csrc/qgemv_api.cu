@@ -197,9 +197,9 @@ void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
 }
 
 int slice_of(int f) { return 8 * sb_bytes(f) + 8 * sb_bytes2(f); }
-// Decoder coefficient bytes per staged superblock (TQ1_0's collapse coefficients, prepared once
-// per CTA); must equal the decoder's kCoefSB.
-int coef_of(int f) { return f == F_TQ10 ? DecTQ10::kCoefSB : 0; }
+// Decoder area bytes per staged superblock (TQ1_0's collapse coefficients and residuals,
+// NVFP4's residuals); must equal the decoder's kCoefSB.
+int coef_of(int f) { return f == F_TQ10 ? DecTQ10::kCoefSB : f == F_NVFP4 ? DecNVFP4::kCoefSB : 0; }
 
 // Packed row bytes of stream 1 / 2, or false when the streaming kernel cannot take the
 // shape (rows must be whole superblocks and 16-byte multiples, at most 16 K-columns).

@@ -6,23 +6,31 @@
 // piece c (64 elements) of superblock col.
 //
 // Activations: the CTA first stages x in shared memory once, converted piece by piece (8
-// elements) into the form the decoders consume (stage_piece); each lane then copies the
-// two 32-element runs of its piece into 32 registers (two values each) and keeps them for
-// the whole kernel, together with the per-chunk factors and sums its offsets need.
+// elements) into the form the decoders consume (stage_piece); each lane then copies its
+// 64 values into 32 registers (two values each) and keeps them for the whole kernel,
+// together with the per-group sums its offsets need.  Every product of an activation and
+// a weight is exact, and every result meets |y - y_ref| <= 2e-3 sum|x w| + 1e-5 for any
+// finite x: the only rounding is fp32 accumulation.
 //
-// Integer-code formats (Q4_K, Q5_K, Q6_K, Q8_0): the codes of a row piece are byte
-// vectors (masked or assembled in place, never shifted down to one code per register)
-// and their dot product with the activations, held as 16-bit fixed point, is taken four
-// bytes at a time by dp2a into int32; the group scale, the group minimum times the
-// activation sum, and the fixed-point exponent are applied once per group.  This is the
-// GPU form of the Q4_K page's "multiply by the masked nibbles and correct once per
-// block" ("Writing a high performant GEMV + dequant for Metal", section "Compute").
-// Block scales use mixed-precision FMAs (sm_100+ `fma.rn.f32.f16`): a small integer v in
-// the low 10 bits of a 16-bit half is the f16 subnormal v * 2^-24, so d (f16) times a
-// 6-bit scale placed there is d*s*2^-24, exact, in one instruction.
+// Integer-code formats (Q4_K, Q5_K, Q6_K, Q8_0) multiply the fp16 activations as they are
+// ("Writing a high performant GEMV + dequant for Metal", section "Compute": the activations
+// are read as floats and multiplied by the masked nibbles).  A code v < 1024 placed in the
+// low bits of a 16-bit half is the f16 subnormal v * 2^-24, so the masked (or assembled)
+// code bytes, moved into 16-bit lanes by a byte permute, are exact f16 operands; the mixed
+// precision FMA (sm_100+ `fma.rn.f32.f16`) forms x * v * 2^-24 exactly and adds it in fp32.
+// Signed codes (Q6_K's q - 32, Q8_0's int8) are made by one exact f16x2 subtraction of the
+// offset in the same subnormal units.  Group scales, minima and the 2^-24 units are applied
+// once per group in fp32.
+//
 // NVFP4 decodes E2M1/E4M3 with the hardware f16 conversions and accumulates f16 x f16
-// products exactly in fp32; TQ1_0 extracts base-3 digits with one rounding FMA each.
+// products exactly in fp32; its bf16 activations are staged as f16 times a power of two per
+// 32-element chunk.  TQ1_0 takes the base-3 digits through the integer collapse, for which
+// the activations are held as integers: two 13-bit fixed-point terms per superblock.  For
+// both, an element that the staged form does not hold exactly leaves a residual (its low
+// bits, an exact f16/bf16 value) that a per-lane correction adds in fp32; typical inputs
+// have none, so the correction costs one predicate test per row.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -40,6 +48,8 @@ __device__ __forceinline__ float bf2f(uint32_t bits16) { return __uint_as_float(
 __device__ __forceinline__ float p2(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
 constexpr float kTwo24 = 16777216.0f;
+constexpr float kTwo44 = 17592186044416.0f;
+constexpr float kTwo48 = 281474976710656.0f;
 
 // c0 += lo(x2) * lo(q2); c1 += hi(x2) * hi(q2)   (f16 x f16 -> exact product, f32 accumulate)
 __device__ __forceinline__ void fma2h(float& c0, float& c1, uint32_t x2, uint32_t q2) {
@@ -57,19 +67,29 @@ __device__ __forceinline__ void mul1x2h(float& r0, float& r1, uint32_t a2, uint3
       : "=f"(r0), "=f"(r1)
       : "r"(a2), "r"(b2));
 }
+// a - b on f16 pairs (subnormals kept: exact whenever the difference is representable)
+__device__ __forceinline__ uint32_t hsub2_raw(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Bytes 0 and 2 / 1 and 3 of a word, each zero-extended into a 16-bit lane.
+__device__ __forceinline__ uint32_t bytes02(uint32_t w) { return __byte_perm(w, 0u, 0x4240); }
+__device__ __forceinline__ uint32_t bytes13(uint32_t w) { return __byte_perm(w, 0u, 0x4341); }
 
 // ------------------------------------------------------------------- activation staging
 // The CTA's copy of x in shared memory: q[K] 16-bit values, e[K/32] one float per 32-element
-// chunk, s[K/16] one int per 16-element half chunk (what they hold depends on the format).
+// chunk, g: the decoder's per-superblock area (kCoefSB bytes each), for decoders that have
+// one.
 struct XStage {
   uint16_t* q;
   float* e;
-  int* s;
-  int* g;  // decoder coefficients (kCoefSB bytes per superblock), for decoders that have them
+  int* g;
 };
 
 // d = c + a.h0 * b.b0 + a.h1 * b.b1 (lo) / a.h0 * b.b2 + a.h1 * b.b3 (hi); a two int16,
-// b four bytes (unsigned or signed).
+// b four unsigned bytes.
 __device__ __forceinline__ int dp2a_lo_u(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -78,16 +98,6 @@ __device__ __forceinline__ int dp2a_lo_u(uint32_t a, uint32_t b, int c) {
 __device__ __forceinline__ int dp2a_hi_u(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp2a_lo_s(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp2a_hi_s(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
@@ -131,48 +141,32 @@ __device__ __forceinline__ uint32_t chunk_max_mag(const uint4& v) {
   return max(m, __shfl_xor_sync(0xffffffffu, m, 2));
 }
 
-// Integer-code formats: a chunk of 32 fp16 activations becomes 16-bit fixed point
-// x_i = round(x * 2^e), e chosen per chunk so that its largest |x| lands in [2^14, 2^15).
-// Values within a factor 16 of that largest one convert exactly (fp16 has 11 significant
-// bits); smaller ones are rounded with error at most 2^-15 of it.  Dot products with the
-// integer codes are then exact int32 sums (dp2a), and the code term and the group-minimum
-// term of a block use the same x_i.
-//  * Conversion is one mixed-precision FMA per value: x (f16) * 2^e1 (f16) + M (f32) with
-//    M = 1.5 * 2^(23 - (e - e1)), whose ulp is 2^(e1 - e), so the sum is rounded to
-//    nearest-even at exactly x * 2^e; its low 16 mantissa bits are then x_i in two's
-//    complement (|x_i| < 2^15 keeps the sum inside M's binade).  e1 = min(e, 15) keeps
-//    the f16 multiplier representable.
-//  * e[chunk] = 2^-e * 2^24 (the 2^24 undoes the subnormal scale factors of the decoders);
-//    s[2 chunk + h] = sum of x_i over half h, by dp2a against byte weights (1, 1).
-__device__ __forceinline__ void int_stage_piece(uint4 v, int i, const XStage& X) {
-  const int e5 = static_cast<int>(chunk_max_mag(v) >> 10);  // f16 biased exponent
-  const int e = 29 - min(e5, 30);                             // in [-1, 29]
-  const int e1 = min(e, 15);
-  const uint32_t s1 = static_cast<uint32_t>(e1 + 15) << 10;  // f16 2^e1
-  const uint32_t s2 = s1 | (s1 << 16);
-  const float M = 1.5f * p2(23 - (e - e1));
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  int hs = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float f0 = M, f1 = M;
-    fma2h(f0, f1, w[k], s2);
-    w[k] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
-    hs = dp2a_lo_u(w[k], 0x0101u, hs);
+// Integer-code formats: x stays fp16, exactly.  Within every four consecutive elements
+// (a, b, c, d) the pairs are stored as (a, c), (b, d): the order in which bytes02 / bytes13
+// deliver the codes of a code word.  With SUMS, e[chunk] = (sum of the chunk's 32 values,
+// in fp32, in a fixed order) * 2^-24, for the group-minimum term.
+template <bool SUMS>
+__device__ __forceinline__ void flt_stage_piece(uint4 v, int i, const XStage& X) {
+  reinterpret_cast<uint4*>(X.q)[i] =
+      make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632), __byte_perm(v.z, v.w, 0x5410),
+                 __byte_perm(v.z, v.w, 0x7632));
+  if constexpr (SUMS) {
+    float s0 = 0.f, s1 = 0.f;
+    fma2h(s0, s1, v.x, 0x3C003C00u);  // times f16 1.0
+    fma2h(s0, s1, v.y, 0x3C003C00u);
+    fma2h(s0, s1, v.z, 0x3C003C00u);
+    fma2h(s0, s1, v.w, 0x3C003C00u);
+    float s = s0 + s1;
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if ((i & 3) == 0) X.e[i >> 2] = s * (1.0f / kTwo24);
   }
-  hs += __shfl_xor_sync(0xffffffffu, hs, 1);
-  reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  if ((i & 1) == 0) X.s[i >> 1] = hs;
-  if ((i & 3) == 0) X.e[i >> 2] = p2(24 - e);
 }
 
 // Lane registers of an integer-code decoder: runs run0 (registers 0..15) and run1 (16..31)
-// of its piece, the factors of their chunks and the four half-chunk sums (run0 halves,
-// then run1 halves).
-struct IntX {
+// of its piece as staged fp16 pairs.
+struct FltX {
   uint32_t xr[32];
-  float xf0, xf1;
-  int xsi[4];
 
   __device__ __forceinline__ void load(const XStage& X, int k0, int k1, bool active) {
     if (active) {
@@ -181,20 +175,9 @@ struct IntX {
       ld_chunk(X.q + k1, b);
 #pragma unroll
       for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
-      const uint32_t ea = static_cast<uint32_t>(__cvta_generic_to_shared(X.e));
-      const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(X.s));
-      xf0 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5)));
-      xf1 = __uint_as_float(lds_u32(ea + 4 * (k1 >> 5)));
-      xsi[0] = static_cast<int>(lds_u32(sa + 4 * (k0 >> 4)));
-      xsi[1] = static_cast<int>(lds_u32(sa + 4 * (k0 >> 4) + 4));
-      xsi[2] = static_cast<int>(lds_u32(sa + 4 * (k1 >> 4)));
-      xsi[3] = static_cast<int>(lds_u32(sa + 4 * (k1 >> 4) + 4));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) xr[i] = 0u;
-      xf0 = xf1 = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) xsi[m] = 0;
     }
   }
 };
@@ -202,20 +185,22 @@ struct IntX {
 // ------------------------------------------------------------------------------- Q4_K
 // Lane piece c = quant bytes [32c, 32c+32): low nibbles are elements 64c + t (group 2c),
 // high nibbles 64c + 32 + t (group 2c+1).  For quant word u (bytes t..t+3, t = 4u) the
-// four low nibbles (word & 0x0F0F0F0F) and the four high nibbles ((word >> 4) & same)
-// are byte vectors that dp2a multiplies with activation pairs (t, t+1), (t+2, t+3) and
-// (32+t, 33+t), (34+t, 35+t): the GPU form of "multiply by the masked nibbles and correct
-// once per block" of the Q4_K page (section "Compute").  Group scales: d (f16) times a
-// 6-bit scale placed as an f16 subnormal gives d*s*2^-24 in one instruction.
-struct DecQ4K : IntX {
+// low nibbles of bytes 0, 2 and of bytes 1, 3 become f16 pairs by one mask each (w and
+// w >> 8), and the high nibbles, left in place (16 q), by one mask each: eight exact
+// products per word, against the activation pairs (t, t+2), (t+1, t+3) and (32+t, 34+t),
+// (33+t, 35+t).  Per group: d*s*sum(x q) - dmin*m*sum(x), the scale/min pairs unpacked
+// from the block header (the page's mask arithmetic) and multiplied by d / dmin with
+// mixed-precision FMAs (a 6-bit value placed as an f16 subnormal gives d*s*2^-24 exactly).
+struct DecQ4K : FltX {
   static constexpr int kSB = 144, kSB2 = 0;
   static constexpr int kCoefSB = 0;
+  static constexpr bool kPrep = false, kResidual = false;
   int c;
   uint32_t sel_s, sel_h, m1, m2, shm;
   uint32_t qoff;   // byte offset of this lane's quants in a block
-  float xs0, xs1;  // activation sums of the two groups
+  float xs0, xs1;  // sums of x over the two groups, times 2^-24 (xs1 also times 16)
 
-  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { flt_stage_piece<true>(v, i, X); }
 
   __device__ __forceinline__ void init(int c_) {
     c = c_;
@@ -230,14 +215,14 @@ struct DecQ4K : IntX {
     shm = (c < 2) ? 0u : 4u;
   }
   __device__ __forceinline__ void load_x_plain(const XStage& X, int sbcol, int c_, bool active) {
-    load(X, 256 * sbcol + 64 * c_, 256 * sbcol + 64 * c_ + 32, active);
-    xs0 = static_cast<float>(xsi[0] + xsi[1]);
-    xs1 = static_cast<float>(xsi[2] + xsi[3]);
+    const int k0 = 256 * sbcol + 64 * c_;
+    load(X, k0, k0 + 32, active);
+    xs0 = active ? X.e[k0 >> 5] : 0.f;
+    xs1 = active ? X.e[(k0 >> 5) + 1] : 0.f;
   }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     load_x_plain(X, sbcol, c_, active);
-    xs1 *= 16.f;  // the high-nibble dot products come out 16 times too large: see row()
-    xf1 *= 0.0625f;
+    xs1 *= 16.f;  // the high-nibble sums come out 16 times too large: see compute()
   }
   // d*s_lo, d*s_hi, dmin*m_lo, dmin*m_hi (times 2^-24) from the block header.
   __device__ __forceinline__ void scales(const uint4 h, float& ds_lo, float& ds_hi, float& dm_lo, float& dm_hi) const {
@@ -246,10 +231,13 @@ struct DecQ4K : IntX {
     mul1x2h(ds_lo, ds_hi, h.x, s2);
     mul1x2h(dm_lo, dm_hi, h.x >> 16, m2v);
   }
-  __device__ __forceinline__ float combine(int lo, int hi, float ds_lo, float ds_hi, float dm_lo, float dm_hi) const {
-    const float t0 = fmaf(ds_lo, static_cast<float>(lo), -dm_lo * xs0);
-    const float t1 = fmaf(ds_hi, static_cast<float>(hi), -dm_hi * xs1);
-    return fmaf(t0, xf0, t1 * xf1);
+  // a_lo = sum(x q) 2^-24 (group 2c), a_hi = sum(x q) 2^-24 times H (group 2c+1); the
+  // result in true units: (ds a - dm xs) carries 2^-48, and the high group 16 / H more.
+  __device__ __forceinline__ float combine(float a_lo, float a_hi, float ds_lo, float ds_hi, float dm_lo, float dm_hi,
+                                           float hi_scale) const {
+    const float t0 = fmaf(ds_lo, a_lo, -dm_lo * xs0);
+    const float t1 = fmaf(ds_hi, a_hi, -dm_hi * xs1);
+    return fmaf(t0, kTwo48, t1 * hi_scale);
   }
 
   // blk: shared-window address of the row's superblock slice (16-byte aligned).
@@ -265,29 +253,27 @@ struct DecQ4K : IntX {
   __device__ __forceinline__ float compute(const Raw& R_) const {
     const uint4 h = R_.h, q0 = R_.q0, q1 = R_.q1;
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      // High nibbles stay in place: dp2a sees 16 q, and 16 * sum(x_i q) still fits int32
-      // (32 values * 240 * 2^15 < 2^28); the factor 16 is folded into xs1 and xf1.
-      const uint32_t L = w[u] & 0x0F0F0F0Fu, H = w[u] & 0xF0F0F0F0u;
-      int& al = (u & 1) ? a1 : a0;
-      int& ah = (u & 1) ? b1 : b0;
-      al = dp2a_lo_u(xr[2 * u], L, al);
-      al = dp2a_hi_u(xr[2 * u + 1], L, al);
-      ah = dp2a_lo_u(xr[16 + 2 * u], H, ah);
-      ah = dp2a_hi_u(xr[16 + 2 * u + 1], H, ah);
+      const uint32_t w8 = w[u] >> 8;
+      const int o = 2 * (u & 1);
+      fma2h(a[o], a[o + 1], xr[2 * u], w[u] & 0x000F000Fu);      // elements t, t+2
+      fma2h(a[o], a[o + 1], xr[2 * u + 1], w8 & 0x000F000Fu);    // t+1, t+3
+      fma2h(b[o], b[o + 1], xr[16 + 2 * u], w[u] & 0x00F000F0u);  // 32+t, 34+t (16 q)
+      fma2h(b[o], b[o + 1], xr[16 + 2 * u + 1], w8 & 0x00F000F0u);
     }
     float ds_lo, ds_hi, dm_lo, dm_hi;
     scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
-    return combine(a0 + a1, b0 + b1, ds_lo, ds_hi, dm_lo, dm_hi);
+    return combine((a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3]), ds_lo, ds_hi, dm_lo, dm_hi, kTwo44);
   }
 };
 
 // ------------------------------------------------------------------------------- Q5_K
-// Q4_K's piece split and activations (quants at byte 48); the fifth bit of element 64c + t
-// (low) / 64c + 32 + t (high) is bit 2c / 2c+1 of qh[t] (qh at byte 16).  A funnel shift
-// brings it to bit 4 of each byte, next to its nibble, before the dot product.
+// Q4_K's piece split, activations and scales (quants at byte 48); the fifth bit of element
+// 64c + t (low) / 64c + 32 + t (high) is bit 2c / 2c+1 of qh[t] (qh at byte 16).  A funnel
+// shift brings it to bit 4 of each byte, next to its nibble; the 5-bit code bytes then
+// become f16 pairs by byte permutes.
 struct DecQ5K : DecQ4K {
   static constexpr int kSB = 176, kSB2 = 0;
   static constexpr int kCoefSB = 0;
@@ -316,21 +302,20 @@ struct DecQ5K : DecQ4K {
     const uint4 qb = lds_v4(blk + 64 + 32 * c);
     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t L = (w[u] & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rl) & 0x10101010u);
       const uint32_t H = ((w[u] >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rh) & 0x10101010u);
-      int& al = (u & 1) ? a1 : a0;
-      int& ah = (u & 1) ? b1 : b0;
-      al = dp2a_lo_u(xr[2 * u], L, al);
-      al = dp2a_hi_u(xr[2 * u + 1], L, al);
-      ah = dp2a_lo_u(xr[16 + 2 * u], H, ah);
-      ah = dp2a_hi_u(xr[16 + 2 * u + 1], H, ah);
+      const int o = 2 * (u & 1);
+      fma2h(a[o], a[o + 1], xr[2 * u], bytes02(L));
+      fma2h(a[o], a[o + 1], xr[2 * u + 1], bytes13(L));
+      fma2h(b[o], b[o + 1], xr[16 + 2 * u], bytes02(H));
+      fma2h(b[o], b[o + 1], xr[16 + 2 * u + 1], bytes13(H));
     }
     float ds_lo, ds_hi, dm_lo, dm_hi;
     scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
-    return combine(a0 + a1, b0 + b1, ds_lo, ds_hi, dm_lo, dm_hi);
+    return combine((a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3]), ds_lo, ds_hi, dm_lo, dm_hi, kTwo48);
   }
 };
 
@@ -338,16 +323,17 @@ struct DecQ5K : DecQ4K {
 // Lane piece c: half H = c>>1, rr = c&1.  Byte ql[64H + 32rr + t] holds, in its low
 // nibble, element 128H + 32rr + t and, in its high nibble, element 128H + 32(rr+2) + t;
 // their top two bits are bits 2rr..2rr+1 / 2rr+4..2rr+5 of qh[32H + t].  The 6-bit codes
-// are assembled bytewise and dotted with dp2a; the -32 offset is removed with the integer
-// sums of the activations of each 16-element scale group.  Blocks are 210 bytes (2-byte
-// aligned), so quant words are read as 16-bit pairs.
-struct DecQ6K : IntX {
+// are assembled bytewise, moved into f16 lanes and made signed (q - 32) by one exact f16
+// subtraction per pair; each 16-element scale group keeps its own sums.  Blocks are 210
+// bytes (2-byte aligned), so quant words are read with a byte permute.
+struct DecQ6K : FltX {
   static constexpr int kSB = 210, kSB2 = 0;
   static constexpr int kCoefSB = 0;
+  static constexpr bool kPrep = false, kResidual = false;
   int c;
   uint32_t rlo, rhi;  // rotate amounts bringing qh bits 2rr / 2rr+4 of each byte to bit 4
 
-  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { flt_stage_piece<false>(v, i, X); }
   __device__ __forceinline__ void init(int c_) {
     c = c_;
     const int rr = c & 1;
@@ -357,9 +343,6 @@ struct DecQ6K : IntX {
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     const int k0 = 256 * sbcol + 128 * (c_ >> 1) + 32 * (c_ & 1);
     load(X, k0, k0 + 64, active);
-    xsi[0] *= 32, xsi[1] *= 32, xsi[2] *= 32, xsi[3] *= 32;
-    xf0 *= 1.0f / kTwo24;
-    xf1 *= 1.0f / kTwo24;
   }
 
   // blk: shared-window address of the row's superblock (2-byte aligned: 210-byte blocks).
@@ -372,45 +355,46 @@ struct DecQ6K : IntX {
     const int H = c >> 1, rr = c & 1;
     const uint32_t ql = blk + 64 * H + 32 * rr;
     const uint32_t qh = blk + 128 + 32 * H;
-    int acc[4] = {0, 0, 0, 0};
+    float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     uint32_t lw[8], hw[8];
     lds_words8_a2(ql, lw);
     lds_words8_a2(qh, hw);
+    constexpr uint32_t k32 = 0x00200020u;  // 32 * 2^-24 in both halves
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t l = lw[u], e = hw[u];
       const uint32_t lo6 = (l & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rlo) & 0x30303030u);
       const uint32_t hi6 = ((l >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e, e, rhi) & 0x30303030u);
       const int g = u >> 2;
-      acc[g] = dp2a_lo_u(xr[2 * u], lo6, acc[g]);
-      acc[g] = dp2a_hi_u(xr[2 * u + 1], lo6, acc[g]);
-      acc[2 + g] = dp2a_lo_u(xr[16 + 2 * u], hi6, acc[2 + g]);
-      acc[2 + g] = dp2a_hi_u(xr[16 + 2 * u + 1], hi6, acc[2 + g]);
+      fma2h(acc[g][0], acc[g][1], xr[2 * u], hsub2_raw(bytes02(lo6), k32));
+      fma2h(acc[g][0], acc[g][1], xr[2 * u + 1], hsub2_raw(bytes13(lo6), k32));
+      fma2h(acc[2 + g][0], acc[2 + g][1], xr[16 + 2 * u], hsub2_raw(bytes02(hi6), k32));
+      fma2h(acc[2 + g][0], acc[2 + g][1], xr[16 + 2 * u + 1], hsub2_raw(bytes13(hi6), k32));
     }
     const uint32_t sc = blk + 192 + 8 * H + 2 * rr;
-    const float d = h2f(lds_u16(blk + 208));
-    const float r0 = fmaf(static_cast<float>(lds_s8(sc)), static_cast<float>(acc[0] - xsi[0]),
-                          static_cast<float>(lds_s8(sc + 1)) * static_cast<float>(acc[1] - xsi[1]));
-    const float r1 = fmaf(static_cast<float>(lds_s8(sc + 4)), static_cast<float>(acc[2] - xsi[2]),
-                          static_cast<float>(lds_s8(sc + 5)) * static_cast<float>(acc[3] - xsi[3]));
-    return d * fmaf(r0, xf0, r1 * xf1);
+    const float d = h2f(lds_u16(blk + 208)) * kTwo24;
+    const float r0 = fmaf(static_cast<float>(lds_s8(sc)), acc[0][0] + acc[0][1],
+                          static_cast<float>(lds_s8(sc + 1)) * (acc[1][0] + acc[1][1]));
+    const float r1 = fmaf(static_cast<float>(lds_s8(sc + 4)), acc[2][0] + acc[2][1],
+                          static_cast<float>(lds_s8(sc + 5)) * (acc[3][0] + acc[3][1]));
+    return d * (r0 + r1);
   }
 };
 
 // ------------------------------------------------------------------------------- Q8_0
 // A superblock is eight 34-byte blocks; lane piece c = blocks 2c and 2c+1 (elements
-// 64c + 32e + j).  The int8 codes are dotted directly with signed dp2a.
-struct DecQ80 : IntX {
+// 64c + 32e + j).  Each int8 code byte is offset to b + 128 (one xor per word), moved into
+// an f16 lane as the subnormal (b + 128) 2^-24 and made b 2^-24 by one exact subtraction.
+struct DecQ80 : FltX {
   static constexpr int kSB = 272, kSB2 = 0;
   static constexpr int kCoefSB = 0;
+  static constexpr bool kPrep = false, kResidual = false;
   int c;
 
-  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { int_stage_piece(v, i, X); }
+  __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { flt_stage_piece<false>(v, i, X); }
   __device__ __forceinline__ void init(int c_) { c = c_; }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     load(X, 256 * sbcol + 64 * c_, 256 * sbcol + 64 * c_ + 32, active);
-    xf0 *= 1.0f / kTwo24;
-    xf1 *= 1.0f / kTwo24;
   }
 
   struct Raw {
@@ -419,23 +403,48 @@ struct DecQ80 : IntX {
   __device__ __forceinline__ Raw fetch(uint32_t blk, uint32_t) const { return Raw{blk}; }
   __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
   __device__ __forceinline__ float row(uint32_t sblk, uint32_t) const {
+    constexpr uint32_t k128 = 0x00800080u;  // 128 * 2^-24 in both halves
     float r[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const uint32_t blk = sblk + 34 * (2 * c + e);
-      int a0 = 0, a1 = 0;
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t qw[8];
       lds_words8_a2(blk + 2, qw);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const uint32_t wd = qw[u];
-        int& a = (u & 1) ? a1 : a0;
-        a = dp2a_lo_s(xr[16 * e + 2 * u], wd, a);
-        a = dp2a_hi_s(xr[16 * e + 2 * u + 1], wd, a);
+        const uint32_t v = qw[u] ^ 0x80808080u;
+        const int o = 2 * (u & 1);
+        fma2h(a[o], a[o + 1], xr[16 * e + 2 * u], hsub2_raw(bytes02(v), k128));
+        fma2h(a[o], a[o + 1], xr[16 * e + 2 * u + 1], hsub2_raw(bytes13(v), k128));
       }
-      r[e] = h2f(lds_u16(blk)) * static_cast<float>(a0 + a1);
+      r[e] = h2f(lds_u16(blk)) * ((a[0] + a[1]) + (a[2] + a[3]));
     }
-    return fmaf(r[0], xf0, r[1] * xf1);
+    return (r[0] + r[1]) * kTwo24;
+  }
+};
+
+// The lane's residual correction: residual values (16-bit, in the lane's own element order
+// j = 0..63) at shared address `ra` and the 64-bit mask of the elements that have one.
+struct Residual {
+  uint32_t rm0, rm1, ra;
+  __device__ __forceinline__ bool any() const { return (rm0 | rm1) != 0u; }
+  __device__ __forceinline__ void clear() { rm0 = rm1 = 0u, ra = 0u; }
+  // Calls f(j, residual bits) for every set element, in increasing j.
+  template <class F>
+  __device__ __forceinline__ void each(F&& f) const {
+    uint32_t m0 = rm0, m1 = rm1;
+    while (m0 | m1) {
+      int j;
+      if (m0) {
+        j = __ffs(m0) - 1;
+        m0 &= m0 - 1u;
+      } else {
+        j = 31 + __ffs(m1);
+        m1 &= m1 - 1u;
+      }
+      f(j, lds_u16(ra + 2u * j));
+    }
   }
 };
 
@@ -446,27 +455,43 @@ struct DecQ80 : IntX {
 // E4M3 are decoded by the hardware conversions to f16 (exact for every code) and f16 x f16
 // products accumulate exactly in fp32.  The bf16 activations are staged per 32-element
 // chunk as f16 times a power of two chosen from the chunk's largest |x| so that every
-// value is below 2^14: f16 then holds each bf16 value exactly (values 2^27 times smaller
-// than the largest lose low bits); the power of two is removed per chunk from the result.
+// value is below 2^14: f16 then holds each bf16 value exactly unless it is more than about
+// 2^30 below the chunk maximum.  Such an element's lost low bits (a bf16 value) are its
+// residual, added by the lane's correction; the power of two is removed per chunk.
+// Decoder area per superblock: residuals [256] (bf16 bits, element order), then one mask
+// byte per 8 elements.
 struct DecNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
-  static constexpr int kCoefSB = 0;
+  static constexpr int kCoefSB = 256 * 2 + 32;
+  static constexpr bool kPrep = false, kResidual = true;
   uint32_t xr[32];
   float xf0, xf1;
   int c;
+  Residual res;
 
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
     const int e8 = static_cast<int>(chunk_max_mag(v) >> 7);  // bf16 biased exponent
     // 2^(e8-127) <= max < 2^(e8-126): scale by 2^(140 - e8) to bring it below 2^14.
-    const float scale = p2(max(-126, min(126, 140 - e8)));
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int sg = max(-126, min(126, 140 - e8));
+    const float scale = p2(sg), inv = p2(-sg);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w}, r[4];
+    uint32_t mask = 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const __half2 h2 = __floats2half2_rn(bf2f(w[k]) * scale, bf2f(w[k] >> 16) * scale);
+      const float x0 = bf2f(w[k]), x1 = bf2f(w[k] >> 16);
+      const __half2 h2 = __floats2half2_rn(x0 * scale, x1 * scale);
+      // what f16 lost: x minus its staged value (an exact bf16 value: low bits of x)
+      const float d0 = x0 - __low2float(h2) * inv, d1 = x1 - __high2float(h2) * inv;
+      r[k] = (__float_as_uint(d0) >> 16) | (__float_as_uint(d1) & 0xFFFF0000u);
+      mask |= (d0 != 0.f ? 1u : 0u) << (2 * k);
+      mask |= (d1 != 0.f ? 1u : 0u) << (2 * k + 1);
       w[k] = *reinterpret_cast<const uint32_t*>(&h2);
     }
     reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    if ((i & 3) == 0) X.e[i >> 2] = 1.0f / scale;
+    if ((i & 3) == 0) X.e[i >> 2] = inv;
+    uint8_t* area = reinterpret_cast<uint8_t*>(X.g) + (i >> 5) * kCoefSB;
+    reinterpret_cast<uint4*>(area)[i & 31] = make_uint4(r[0], r[1], r[2], r[3]);
+    area[512 + (i & 31)] = static_cast<uint8_t>(mask);
   }
   __device__ __forceinline__ void init(int c_) { c = c_; }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
@@ -480,10 +505,15 @@ struct DecNVFP4 {
       const uint32_t ea = static_cast<uint32_t>(__cvta_generic_to_shared(X.e));
       xf0 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5)));
       xf1 = __uint_as_float(lds_u32(ea + 4 * (k0 >> 5) + 4));
+      const uint32_t area = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + sbcol * kCoefSB;
+      res.rm0 = lds_u32(area + 512 + 8 * c_);
+      res.rm1 = lds_u32(area + 512 + 8 * c_ + 4);
+      res.ra = area + 128 * c_;
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) xr[i] = 0u;
       xf0 = xf1 = 0.f;
+      res.clear();
     }
   }
 
@@ -536,6 +566,19 @@ struct DecNVFP4 {
     }
     return fmaf(r[0], xf0, r[1] * xf1);
   }
+  __device__ __forceinline__ bool has_residual() const { return res.any(); }
+  // Sum of residual x element j times its weight e2m1 * |e4m3|, exact products in fp32.
+  __device__ __forceinline__ float correction(uint32_t nib, uint32_t sc) const {
+    float acc = 0.f;
+    res.each([&](int j, uint32_t rbits) {
+      const uint32_t byte = lds_u8(nib + 32 * c + (j >> 1));
+      const uint32_t e = e2m1x2(byte);
+      const float wv = h2f((j & 1) ? (e >> 16) : e);
+      const float sv = h2f(e4m3x2(lds_u8(sc + 4 * c + (j >> 4)) & 0x7Fu));
+      acc = fmaf(bf2f(rbits), wv * sv, acc);
+    });
+    return acc;
+  }
 };
 
 // ------------------------------------------------------------------------------- TQ1_0
@@ -543,119 +586,178 @@ struct DecNVFP4 {
 // digits n = 0..4 weigh activations y_0..y_4: sum_n y_n t_n(b) = sum_{k=1..5} g_k F_k(b)
 // with F_k(b) = floor(3^k b / 256), g_k = y_{k-1} - 3 y_k, y_5 = 0; qh bytes carry four
 // digits, so their y_4 is 0 ("metal: TQ1_0 kernel performance", section 1, the zero-padded
-// collapse).  Here everything is integer: the activations are 13-bit fixed point with one
-// exponent per superblock, so every g_k fits int16; F_k of four bytes at once comes from
-// multiplying the even and the odd bytes, spread into 16-bit lanes, by 3 (k times; b 3^k <
-// 2^16 never carries into the next lane) and picking byte 1 of each lane; dp2a then takes
-// the dot products with the int16 g pairs.
+// collapse).  Everything here is integer: F_k of four bytes at once comes from multiplying
+// the even and the odd bytes, spread into 16-bit lanes, by 3 (k times; b 3^k < 2^16 never
+// carries into the next lane) and picking byte 1 of each lane; dp2a then takes the dot
+// products with int16 g pairs.  The activations are held as two 13-bit fixed-point terms
+// per superblock: x 2^e = hi + lo 2^-13 (+ a residual below that grid), e chosen so that
+// the superblock's largest |x| lands in [2^12, 2^13); |hi| <= 8188 and |lo| <= 4096 keep
+// every g_k in int16.  For activations whose largest |x| is below 4 the two terms hold every
+// fp16 value exactly; finer bits leave a residual, which the lane's correction adds.
 struct DecTQ10 {
   static constexpr int kSB = 54, kSB2 = 0;
-  uint32_t gw[3][5][2];  // [word][k-1]: g of bytes 0,1 and of bytes 2,3 as int16 pairs
-  int gq[4];             // qh byte: g_k, k = 1..4
-  int xsum;              // sum of the lane's 64 fixed-point activations
-  float xf;              // 2^-e of the superblock
+  static constexpr bool kPrep = true, kResidual = true;
+  // Decoder area per superblock: lo [256] (int16, element order) at 0, residuals [256] (f16
+  // bits, element order) at 512, then per lane piece 96 words at 1024 + 384 c: the hi term's
+  // coefficients (40 words: g of word w at 10 w + 2 (k - 1) + h, h = bytes 0,1 / 2,3 as int16
+  // pairs; the qh g_k at 30 + k - 1; partial sums of y at 34..37), the lo term's at 40..79,
+  // and the residual mask bits of the four items at 80..83 (lane element order j: 5 b + n for
+  // qs byte b and digit n, 60 + n for the qh digits).  X.q holds hi (int16, element order).
+  static constexpr int kCoefSB = 1024 + 4 * 384;
+  uint32_t gw[2][3][5][2];  // [term][word][k-1]: g of bytes 0,1 and of bytes 2,3 as int16 pairs
+  int gq[2][4];             // qh byte: g_k, k = 1..4
+  int xsum[2];              // sums of the lane's 64 fixed-point activations
+  float xf, xf_lo;          // 2^-e and 2^-(e+13) of the superblock
   int c;
+  Residual res;             // res.ra: the superblock's element-order residuals
 
   __device__ __forceinline__ static int elem_of(int p, int n) {
     if (p < 32) return 32 * n + p;
     if (p < 48) return 160 + 16 * n + (p - 32);
     return 240 + 4 * n + (p - 48);
   }
-  // 13-bit fixed point per superblock: the 32 pieces of a superblock are the 32 lanes of one
-  // warp, which share the largest magnitude by shuffles.  Same conversion as the integer
-  // formats (one mixed-precision FMA per value), with the maximum landing in [2^12, 2^13).
+  // The 32 pieces of a superblock are the 32 lanes of one warp, which share the largest
+  // magnitude by shuffles; each thread then splits its 8 values: hi = rint(x 2^e), lo =
+  // rint((x 2^e - hi) 2^13), residual = x - (hi + lo 2^-13) 2^-e (all exact in fp32; the
+  // residual is a part of x's own bits, so an exact f16 value).  e[sb] = 2^e.
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
     uint32_t m2 = vmax_u16x2(vmax_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), vmax_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     const int e5 = static_cast<int>(m >> 10);
-    const int e = 27 - min(e5, 30);  // in [-3, 27]
-    const int e1 = min(e, 15);
-    const uint32_t s1 = static_cast<uint32_t>(e1 + 15) << 10;
-    const uint32_t s2 = s1 | (s1 << 16);
-    const float M = 1.5f * p2(23 - (e - e1));
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int e = 27 - min(e5, 30);  // in [-3, 27]: max * 2^e in [2^12, 2^13)
+    const float sc = p2(e), isc = p2(-e - 13);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hw[4], lw[4], rw[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float f0 = M, f1 = M;
-      fma2h(f0, f1, w[k], s2);
-      w[k] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
+      uint32_t hh = 0u, ll = 0u, rr = 0u;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float xf = h2f(w[k] >> (16 * hf)) * sc;  // exact
+        const float hi = rintf(xf);
+        const float r13 = (xf - hi) * 8192.f;  // exact
+        const float lo = rintf(r13);
+        const float rx = (r13 - lo) * isc;  // exact
+        hh |= (static_cast<uint32_t>(static_cast<int>(hi)) & 0xFFFFu) << (16 * hf);
+        ll |= (static_cast<uint32_t>(static_cast<int>(lo)) & 0xFFFFu) << (16 * hf);
+        rr |= static_cast<uint32_t>(__half_as_ushort(__float2half_rn(rx))) << (16 * hf);
+      }
+      hw[k] = hh, lw[k] = ll, rw[k] = rr;
     }
-    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    if ((i & 31) == 0) X.e[i >> 5] = p2(-e);
+    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    uint8_t* area = reinterpret_cast<uint8_t*>(X.g) + (i >> 5) * kCoefSB;
+    reinterpret_cast<uint4*>(area)[i & 31] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    reinterpret_cast<uint4*>(area + 512)[i & 31] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
+    if ((i & 31) == 0) X.e[i >> 5] = sc;
   }
   __device__ __forceinline__ void init(int c_) { c = c_; }
-  // Collapse coefficients of every lane piece of the staged x, computed once per CTA by all
-  // its threads (every warp of the CTA reads the same pieces).  Item (superblock, piece c,
-  // part): parts 0..2 are the piece's qs words, part 3 its qh byte; each writes its g_k and
-  // its partial sum of x into the piece's 40 words: g of word w at 10 w + 2 (k - 1) + h (h: bytes
-  // 0,1 / 2,3 as int16 pairs), the qh g_k at 30 + k - 1, the four partial sums at 34..37.
-  static constexpr int kCoefSB = 4 * 160;
+  // The collapse coefficients and residual masks of every lane piece of the staged x,
+  // computed once per CTA by all its threads (every warp of the CTA reads the same pieces).
+  // Item (superblock, piece c, part): parts 0..2 are the piece's qs words, part 3 its qh byte.
   __device__ static void prep(const XStage& X, int nsb, int tid, int nthreads) {
     const uint32_t q0 = static_cast<uint32_t>(__cvta_generic_to_shared(X.q));
+    const uint32_t a0 = static_cast<uint32_t>(__cvta_generic_to_shared(X.g));
     for (int it = tid; it < 16 * nsb; it += nthreads) {
       const int sb = it >> 4, c = (it >> 2) & 3, part = it & 3;
-      const uint32_t qa = q0 + 512u * sb;
-      auto xi = [&](int p, int n) -> int { return static_cast<int>(static_cast<int16_t>(lds_u16(qa + 2 * elem_of(p, n)))); };
-      int* g = X.g + (4 * sb + c) * 40;
-      int xs = 0;
+      const uint32_t qa = q0 + 512u * sb, area = a0 + static_cast<uint32_t>(kCoefSB) * sb;
+      int* g = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(X.g) + kCoefSB * sb + 1024 + 384 * c);
+      uint32_t mbits = 0u;
+      int xs[2] = {0, 0};
+      // element (p, n): hi and lo terms, and its mask bit at lane element index j
+      auto get = [&](int p, int n, int j, int& yh, int& yl) {
+        const uint32_t off = 2u * elem_of(p, n);
+        yh = static_cast<int>(static_cast<int16_t>(lds_u16(qa + off)));
+        yl = static_cast<int>(static_cast<int16_t>(lds_u16(area + off)));
+        if (lds_u16(area + 512 + off) & 0x7FFFu) mbits |= 1u << (part < 3 ? j - 20 * part : j - 60);
+      };
       if (part < 3) {
-        int gg[4][5];
+        int gg[2][4][5];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int p = 12 * c + 4 * part + j;
-          int y[6];
+        for (int b = 0; b < 4; ++b) {
+          const int p = 12 * c + 4 * part + b;
+          int y[2][6];
 #pragma unroll
-          for (int n = 0; n < 5; ++n) y[n] = xi(p, n), xs += y[n];
-          y[5] = 0;
+          for (int n = 0; n < 5; ++n) {
+            get(p, n, 5 * (4 * part + b) + n, y[0][n], y[1][n]);
+            xs[0] += y[0][n], xs[1] += y[1][n];
+          }
 #pragma unroll
-          for (int k = 1; k <= 5; ++k) gg[j][k - 1] = y[k - 1] - 3 * y[k];
+          for (int t = 0; t < 2; ++t) {
+            y[t][5] = 0;
+#pragma unroll
+            for (int k = 1; k <= 5; ++k) gg[t][b][k - 1] = y[t][k - 1] - 3 * y[t][k];
+          }
         }
 #pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          g[10 * part + 2 * k] = static_cast<int>((static_cast<uint32_t>(gg[0][k]) & 0xFFFFu) |
-                                                  (static_cast<uint32_t>(gg[1][k]) << 16));
-          g[10 * part + 2 * k + 1] = static_cast<int>((static_cast<uint32_t>(gg[2][k]) & 0xFFFFu) |
-                                                      (static_cast<uint32_t>(gg[3][k]) << 16));
-        }
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int k = 0; k < 5; ++k) {
+            g[40 * t + 10 * part + 2 * k] = static_cast<int>((static_cast<uint32_t>(gg[t][0][k]) & 0xFFFFu) |
+                                                             (static_cast<uint32_t>(gg[t][1][k]) << 16));
+            g[40 * t + 10 * part + 2 * k + 1] = static_cast<int>((static_cast<uint32_t>(gg[t][2][k]) & 0xFFFFu) |
+                                                                 (static_cast<uint32_t>(gg[t][3][k]) << 16));
+          }
       } else {
-        int y[5];
+        int y[2][5];
 #pragma unroll
-        for (int n = 0; n < 4; ++n) y[n] = xi(48 + c, n), xs += y[n];
-        y[4] = 0;
+        for (int n = 0; n < 4; ++n) {
+          get(48 + c, n, 60 + n, y[0][n], y[1][n]);
+          xs[0] += y[0][n], xs[1] += y[1][n];
+        }
 #pragma unroll
-        for (int k = 1; k <= 4; ++k) g[30 + k - 1] = y[k - 1] - 3 * y[k];
+        for (int t = 0; t < 2; ++t) {
+          y[t][4] = 0;
+#pragma unroll
+          for (int k = 1; k <= 4; ++k) g[40 * t + 30 + k - 1] = y[t][k - 1] - 3 * y[t][k];
+        }
       }
-      g[34 + part] = xs;
+      g[34 + part] = xs[0];
+      g[40 + 34 + part] = xs[1];
+      g[80 + part] = static_cast<int>(mbits);
     }
   }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     if (active) {
-      const uint32_t ga = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + 160u * (4 * sbcol + c_);
-      uint32_t v[40];
+      const uint32_t area = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + static_cast<uint32_t>(kCoefSB) * sbcol;
+      const uint32_t ga = area + 1024 + 384 * c_;
 #pragma unroll
-      for (int i = 0; i < 10; ++i) {
-        const uint4 t = lds_v4(ga + 16 * i);
-        v[4 * i] = t.x, v[4 * i + 1] = t.y, v[4 * i + 2] = t.z, v[4 * i + 3] = t.w;
+      for (int t = 0; t < 2; ++t) {
+        uint32_t v[40];
+#pragma unroll
+        for (int i = 0; i < 10; ++i) {
+          const uint4 q = lds_v4(ga + 160 * t + 16 * i);
+          v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+        }
+#pragma unroll
+        for (int w = 0; w < 3; ++w)
+#pragma unroll
+          for (int k = 0; k < 5; ++k) gw[t][w][k][0] = v[10 * w + 2 * k], gw[t][w][k][1] = v[10 * w + 2 * k + 1];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gq[t][k] = static_cast<int>(v[30 + k]);
+        xsum[t] = static_cast<int>(v[34]) + static_cast<int>(v[35]) + static_cast<int>(v[36]) + static_cast<int>(v[37]);
       }
-#pragma unroll
-      for (int w = 0; w < 3; ++w)
-#pragma unroll
-        for (int k = 0; k < 5; ++k) gw[w][k][0] = v[10 * w + 2 * k], gw[w][k][1] = v[10 * w + 2 * k + 1];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) gq[k] = static_cast<int>(v[30 + k]);
-      xsum = static_cast<int>(v[34]) + static_cast<int>(v[35]) + static_cast<int>(v[36]) + static_cast<int>(v[37]);
-      xf = X.e[sbcol];
+      const uint4 mb = lds_v4(ga + 320);
+      // item masks: bits j in [0,20), [20,40), [40,60), [60,64)
+      res.rm0 = mb.x | (mb.y << 20);
+      res.rm1 = (mb.y >> 12) | (mb.z << 8) | (mb.w << 28);
+      res.ra = area + 512;
+      xf = 1.0f / X.e[sbcol];
+      xf_lo = xf * (1.0f / 8192.f);
     } else {
 #pragma unroll
-      for (int w = 0; w < 3; ++w)
+      for (int t = 0; t < 2; ++t) {
 #pragma unroll
-        for (int k = 0; k < 5; ++k) gw[w][k][0] = gw[w][k][1] = 0u;
+        for (int w = 0; w < 3; ++w)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) gq[k] = 0;
-      xsum = 0;
-      xf = 0.f;
+          for (int k = 0; k < 5; ++k) gw[t][w][k][0] = gw[t][w][k][1] = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gq[t][k] = 0;
+        xsum[t] = 0;
+      }
+      xf = xf_lo = 0.f;
+      res.clear();
     }
   }
 
@@ -667,7 +769,7 @@ struct DecTQ10 {
   // blk: shared-window address of the row's block (2-byte aligned: 54-byte blocks).
   __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
     const uint32_t q = blk + 12 * c;
-    int acc = 0;
+    int acc = 0, acl = 0;
 #pragma unroll
     for (int w = 0; w < 3; ++w) {
       const uint32_t W = lds_u16(q + 4 * w) | (lds_u16(q + 4 * w + 2) << 16);
@@ -678,18 +780,47 @@ struct DecTQ10 {
         pe *= 3u;
         po *= 3u;
         const uint32_t F = __byte_perm(pe, po, 0x7351);  // F_k of bytes 0..3
-        acc = dp2a_lo_u(gw[w][k][0], F, acc);
-        acc = dp2a_hi_u(gw[w][k][1], F, acc);
+        acc = dp2a_lo_u(gw[0][w][k][0], F, acc);
+        acc = dp2a_hi_u(gw[0][w][k][1], F, acc);
+        acl = dp2a_lo_u(gw[1][w][k][0], F, acl);
+        acl = dp2a_hi_u(gw[1][w][k][1], F, acl);
       }
     }
     uint32_t pq = lds_u8(blk + 48 + c);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       pq *= 3u;
-      acc += gq[k] * static_cast<int>(pq >> 8);
+      const int f = static_cast<int>(pq >> 8);
+      acc += gq[0][k] * f;
+      acl += gq[1][k] * f;
     }
     const float d = h2f(lds_u16(blk + 52));
-    return d * static_cast<float>(acc - xsum) * xf;
+    return d * fmaf(static_cast<float>(acc - xsum[0]), xf, static_cast<float>(acl - xsum[1]) * xf_lo);
+  }
+  __device__ __forceinline__ bool has_residual() const { return res.any(); }
+  // d times the sum of residual x element j times its weight t - 1, in fp32.
+  __device__ __forceinline__ float correction(uint32_t blk, uint32_t) const {
+    float acc = 0.f;
+    uint32_t m0 = res.rm0, m1 = res.rm1;
+    while (m0 | m1) {
+      int j;
+      if (m0) {
+        j = __ffs(m0) - 1;
+        m0 &= m0 - 1u;
+      } else {
+        j = 31 + __ffs(m1);
+        m1 &= m1 - 1u;
+      }
+      const bool qh = j >= 60;
+      const int p = qh ? 48 + c : 12 * c + j / 5;
+      const int n = qh ? j - 60 : j % 5;
+      const uint32_t b = lds_u8(blk + p);
+      uint32_t pw = 1u;
+      for (int i = 0; i < n; ++i) pw *= 3u;
+      const int t = static_cast<int>((3u * pw * b) >> 8) - 3 * static_cast<int>((pw * b) >> 8);
+      acc = fmaf(h2f(lds_u16(res.ra + 2u * elem_of(p, n))), static_cast<float>(t - 1), acc);
+    }
+    return h2f(lds_u16(blk + 52)) * acc;
   }
 };
 

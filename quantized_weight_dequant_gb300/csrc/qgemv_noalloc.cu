@@ -146,7 +146,7 @@ extern "C" qgemv_status_t qgemv_run_noalloc(qgemv_format_t fmt, const void* x, c
   const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
   auto rix = [](int r) { return r == 1 ? 0 : r == 2 ? 1 : 2; };
   auto limit = [&](int d, int r) { return std::min(s->dyn_smem_max[f][rix(r)][d - 2], cap); };
-  const int coef = f == F_TQ10 ? DecTQ10::kCoefSB : 0;
+  const int coef = f == F_TQ10 ? DecTQ10::kCoefSB : f == F_NVFP4 ? DecNVFP4::kCoefSB : 0;
   auto smem_of = [&](int d, int r) { return stream_smem(P, d, r, slice, Wk, 0, Kx, coef).total; };
   while (smem_of(D, R) > limit(D, R) && (D > 2 || R > 1)) {
     if (D > 2)

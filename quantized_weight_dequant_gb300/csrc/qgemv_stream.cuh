@@ -18,7 +18,9 @@
 //  * The Wk partial sums of a row are added in a fixed order in shared memory at the end,
 //    so results are bitwise reproducible.
 //  * x is staged once per CTA in shared memory, converted there to the decoders' form
-//    (fixed point for the integer-code formats), then copied by each lane to registers.
+//    (exact fp16 pairs for the integer-code formats, scaled f16 for NVFP4, integer
+//    collapse coefficients for TQ1_0), then copied by each lane to registers.  Elements
+//    the staged form does not hold exactly are corrected per lane from their residuals.
 //  * Under programmatic dependent launch the first weight stages are requested before the
 //    wait for the previous kernel (weights are not written by it); x is read after it.
 //  * The body is shared by the single-matrix kernel (fp32 row sums stored as they are) and
@@ -111,10 +113,10 @@ __host__ __device__ constexpr int slice_bytes() {
 }
 
 // Shared memory: [rings: warps * D * R * slice][reduction buffer][x staging: q (2K bytes),
-// e (K/32 floats), s (K/16 ints)][decoder coefficients: coef_sb bytes per superblock of the
-// staged x][never-completing barrier], each part 16-byte aligned.
+// e (K/32 floats)][decoder area: coef_sb bytes per superblock of the staged x][never-
+// completing barrier], each part 16-byte aligned.
 struct StreamSmem {
-  size_t red, xq, xe, xs, xc, bar, total;
+  size_t red, xq, xe, xc, bar, total;
 };
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
 __host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int slice, int Wk, int red_rows, int K,
@@ -123,8 +125,7 @@ __host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int s
   m.red = static_cast<size_t>(warps) * D * R * slice;
   m.xq = align16(m.red + (Wk > 1 ? static_cast<size_t>(red_rows) * Wk * 4 : 0));
   m.xe = align16(m.xq + static_cast<size_t>(K) * 2);
-  m.xs = align16(m.xe + static_cast<size_t>(K / 32) * 4);
-  m.xc = align16(m.xs + static_cast<size_t>(K / 16) * 4);
+  m.xc = align16(m.xe + static_cast<size_t>(K / 32) * 4);
   m.bar = align16(m.xc + static_cast<size_t>(K / 256) * coef_sb);
   m.total = m.bar + 16;
   return m;
@@ -220,7 +221,7 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   uint8_t* ring = smem + static_cast<size_t>(warp) * D * STAGE;
   float* red = reinterpret_cast<float*>(smem + L.red);
   const XStage X{reinterpret_cast<uint16_t*>(smem + L.xq), reinterpret_cast<float*>(smem + L.xe),
-                 reinterpret_cast<int*>(smem + L.xs), reinterpret_cast<int*>(smem + L.xc)};
+                 reinterpret_cast<int*>(smem + L.xc)};
   uint64_t* never_bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
   pdl_launch_dependents();  // the next kernel may start copying its weights right away
@@ -360,7 +361,7 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   }
   __syncthreads();
   QG_TRACE(2);
-  if constexpr (Dec::kCoefSB > 0) {  // per-CTA decoder coefficients of the staged x
+  if constexpr (Dec::kPrep) {  // per-CTA decoder coefficients of the staged x
     Dec::prep(X, (pc1 - pc0) / 32, threadIdx.x, blockDim.x);
     __syncthreads();
   }
@@ -391,6 +392,14 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
     float v[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) v[r] = dec.compute(raw[r]);
+    if constexpr (Dec::kResidual) {
+      // Elements of this lane's x that the staged form does not hold exactly (none for
+      // typical inputs): their residuals times their weights, from the same ring slot.
+      if (dec.has_residual()) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] += dec.correction(cs + lo1 + r * SLICE, cs + lo2 + r * SLICE);
+      }
+    }
     __syncwarp();  // every lane is done with this slot before it is refilled
     is = cs;
     cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;

@@ -401,3 +401,25 @@ def test_swiglu_gates_the_up_rows_with_silu_of_the_gate_rows(fmt):
     # the two matrices play different roles: swapping them changes the result
     swapped = oracle.swiglu(fmt, x, Wu, Wg, N, K)["h"]
     assert not np.allclose(swapped, out["h"], rtol=1e-3)
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.NVFP4, synth.TQ1_0, synth.Q5_K, synth.Q6_K, synth.Q8_0])
+def test_zero_weight_column_edit_is_exact(fmt):
+    """The wide-range tests' weight edit: the chosen columns dequantise (by the oracle) to
+    exactly zero in every row, every other weight outside the edited Q4_K/Q5_K groups keeps
+    its value, and the edited bytes still decode with the oracle's layout."""
+    from wide_range import zero_weight_columns
+    N, K = 3, 512
+    W = synth.make_weights(fmt, N, K, seed=5 + fmt)
+    cols = np.array([0, 37, 64, 255, 256, 300, 511])
+    W2 = zero_weight_columns(fmt, W, N, K, cols)
+    a = oracle.dequant_rows(fmt, W, N, K, np.arange(N))
+    b = oracle.dequant_rows(fmt, W2, N, K, np.arange(N))
+    assert np.all(b[:, cols] == 0.0)
+    keep = np.ones(K, dtype=bool)
+    if fmt in (synth.Q4_K, synth.Q5_K):  # the group minimum of an edited column's group is 0
+        for c in cols:
+            keep[(c // 32) * 32:(c // 32) * 32 + 32] = False
+    else:
+        keep[cols] = False
+    assert np.array_equal(a[:, keep], b[:, keep])
