@@ -22,12 +22,13 @@
 // offset in the same subnormal units.  Group scales, minima and the 2^-24 units are applied
 // once per group in fp32.
 //
+// TQ1_0 also keeps x as fp16: its base-3 digits, stepped out of the packed bytes two at a
+// time, become the exact f16 operands (t - 1) 2^-16 of the same FMAs.
+//
 // NVFP4 decodes E2M1/E4M3 with the hardware f16 conversions and accumulates f16 x f16
 // products exactly in fp32; its bf16 activations are staged as f16 times a power of two per
-// 32-element chunk.  TQ1_0 takes the base-3 digits through the integer collapse, for which
-// the activations are held as integers: two 13-bit fixed-point terms per superblock.  For
-// both, an element that the staged form does not hold exactly leaves a residual (its low
-// bits, an exact f16/bf16 value) that a per-lane correction adds in fp32; typical inputs
+// 32-element chunk.  An element that this form does not hold exactly leaves a residual (its
+// low bits, an exact bf16 value) that a per-lane correction adds in fp32; typical inputs
 // have none, so the correction costs one predicate test per row.
 #pragma once
 #include <cuda_bf16.h>
@@ -582,183 +583,56 @@ struct DecNVFP4 {
 };
 
 // ------------------------------------------------------------------------------- TQ1_0
-// Lane piece c = qs bytes [12c, 12c+12) (three words) and qh byte c.  For a byte b whose
-// digits n = 0..4 weigh activations y_0..y_4: sum_n y_n t_n(b) = sum_{k=1..5} g_k F_k(b)
-// with F_k(b) = floor(3^k b / 256), g_k = y_{k-1} - 3 y_k, y_5 = 0; qh bytes carry four
-// digits, so their y_4 is 0 ("metal: TQ1_0 kernel performance", section 1, the zero-padded
-// collapse).  Everything here is integer: F_k of four bytes at once comes from multiplying
-// the even and the odd bytes, spread into 16-bit lanes, by 3 (k times; b 3^k < 2^16 never
-// carries into the next lane) and picking byte 1 of each lane; dp2a then takes the dot
-// products with int16 g pairs.  The activations are held as two 13-bit fixed-point terms
-// per superblock: x 2^e = hi + lo 2^-13 (+ a residual below that grid), e chosen so that
-// the superblock's largest |x| lands in [2^12, 2^13); |hi| <= 8188 and |lo| <= 4096 keep
-// every g_k in int16.  For activations whose largest |x| is below 4 the two terms hold every
-// fp16 value exactly; finer bits leave a residual, which the lane's correction adds.
-struct DecTQ10 {
+// Lane piece c = qs bytes [12c, 12c+12) (three words) and qh byte c: 60 + 4 elements.  The
+// digit of weight n of byte b is floor(3^(n+1) b / 256) mod 3 ("metal: TQ1_0 kernel
+// performance", section 1), taken one step at a time: with r = b, r3 = 3 r gives the digit
+// t = r3 >> 8 (0, 1 or 2) and r = r3 & 255 for the next one.  Bytes 0, 2 and bytes 1, 3 of
+// a word share the 16-bit lanes of one register, so one multiply steps two bytes (3 r < 2^16
+// never carries into the next lane).  t stays in bits 8..9 of its lane: as an f16 subnormal
+// that is t 2^-16, made (t - 1) 2^-16 by one exact f16 subtraction, and its product with
+// the fp16 activation is exact (mixed-precision FMA, fp32 accumulation); d and 2^16 are
+// applied once per row.  The qh byte carries four digits: its two lanes start at digits 0
+// and 2 (b and 9b mod 256) and take two steps.
+// Staging: x is kept as fp16, each superblock in its own 528-byte slot of the decoder area
+// (256 values and 16 bytes of padding, so the slots of the eight superblocks a warp reads
+// start on different banks); each lane gathers its 64 values once, in the order compute()
+// takes them: register 10 w + 2 n + h holds the digit-n elements of bytes h and h + 2 of
+// word w, registers 30 / 31 the qh digits (0, 2) / (1, 3).
+struct DecTQ10 : FltX {
   static constexpr int kSB = 54, kSB2 = 0;
-  static constexpr bool kPrep = true, kResidual = true;
-  // Decoder area per superblock: lo [256] (int16, element order) at 0, residuals [256] (f16
-  // bits, element order) at 512, then per lane piece 96 words at 1024 + 384 c: the hi term's
-  // coefficients (40 words: g of word w at 10 w + 2 (k - 1) + h, h = bytes 0,1 / 2,3 as int16
-  // pairs; the qh g_k at 30 + k - 1; partial sums of y at 34..37), the lo term's at 40..79,
-  // and the residual mask bits of the four items at 80..83 (lane element order j: 5 b + n for
-  // qs byte b and digit n, 60 + n for the qh digits).  X.q holds hi (int16, element order).
-  static constexpr int kCoefSB = 1024 + 4 * 384;
-  uint32_t gw[2][3][5][2];  // [term][word][k-1]: g of bytes 0,1 and of bytes 2,3 as int16 pairs
-  int gq[2][4];             // qh byte: g_k, k = 1..4
-  int xsum[2];              // sums of the lane's 64 fixed-point activations
-  float xf, xf_lo;          // 2^-e and 2^-(e+13) of the superblock
+  static constexpr int kCoefSB = 528;
+  static constexpr bool kPrep = false, kResidual = false;
   int c;
-  Residual res;             // res.ra: the superblock's element-order residuals
 
+  // Element of the superblock that digit n of byte p weighs (p < 48: qs, else qh).
   __device__ __forceinline__ static int elem_of(int p, int n) {
     if (p < 32) return 32 * n + p;
     if (p < 48) return 160 + 16 * n + (p - 32);
     return 240 + 4 * n + (p - 48);
   }
-  // The 32 pieces of a superblock are the 32 lanes of one warp, which share the largest
-  // magnitude by shuffles; each thread then splits its 8 values: hi = rint(x 2^e), lo =
-  // rint((x 2^e - hi) 2^13), residual = x - (hi + lo 2^-13) 2^-e (all exact in fp32; the
-  // residual is a part of x's own bits, so an exact f16 value).  e[sb] = 2^e.
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
-    uint32_t m2 = vmax_u16x2(vmax_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), vmax_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const int e5 = static_cast<int>(m >> 10);
-    const int e = 27 - min(e5, 30);  // in [-3, 27]: max * 2^e in [2^12, 2^13)
-    const float sc = p2(e), isc = p2(-e - 13);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t hw[4], lw[4], rw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t hh = 0u, ll = 0u, rr = 0u;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float xf = h2f(w[k] >> (16 * hf)) * sc;  // exact
-        const float hi = rintf(xf);
-        const float r13 = (xf - hi) * 8192.f;  // exact
-        const float lo = rintf(r13);
-        const float rx = (r13 - lo) * isc;  // exact
-        hh |= (static_cast<uint32_t>(static_cast<int>(hi)) & 0xFFFFu) << (16 * hf);
-        ll |= (static_cast<uint32_t>(static_cast<int>(lo)) & 0xFFFFu) << (16 * hf);
-        rr |= static_cast<uint32_t>(__half_as_ushort(__float2half_rn(rx))) << (16 * hf);
-      }
-      hw[k] = hh, lw[k] = ll, rw[k] = rr;
-    }
-    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    uint8_t* area = reinterpret_cast<uint8_t*>(X.g) + (i >> 5) * kCoefSB;
-    reinterpret_cast<uint4*>(area)[i & 31] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    reinterpret_cast<uint4*>(area + 512)[i & 31] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
-    if ((i & 31) == 0) X.e[i >> 5] = sc;
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(X.g) + kCoefSB * (i >> 5) + 16 * (i & 31)) = v;
   }
   __device__ __forceinline__ void init(int c_) { c = c_; }
-  // The collapse coefficients and residual masks of every lane piece of the staged x,
-  // computed once per CTA by all its threads (every warp of the CTA reads the same pieces).
-  // Item (superblock, piece c, part): parts 0..2 are the piece's qs words, part 3 its qh byte.
-  __device__ static void prep(const XStage& X, int nsb, int tid, int nthreads) {
-    const uint32_t q0 = static_cast<uint32_t>(__cvta_generic_to_shared(X.q));
-    const uint32_t a0 = static_cast<uint32_t>(__cvta_generic_to_shared(X.g));
-    for (int it = tid; it < 16 * nsb; it += nthreads) {
-      const int sb = it >> 4, c = (it >> 2) & 3, part = it & 3;
-      const uint32_t qa = q0 + 512u * sb, area = a0 + static_cast<uint32_t>(kCoefSB) * sb;
-      int* g = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(X.g) + kCoefSB * sb + 1024 + 384 * c);
-      uint32_t mbits = 0u;
-      int xs[2] = {0, 0};
-      // element (p, n): hi and lo terms, and its mask bit at lane element index j
-      auto get = [&](int p, int n, int j, int& yh, int& yl) {
-        const uint32_t off = 2u * elem_of(p, n);
-        yh = static_cast<int>(static_cast<int16_t>(lds_u16(qa + off)));
-        yl = static_cast<int>(static_cast<int16_t>(lds_u16(area + off)));
-        if (lds_u16(area + 512 + off) & 0x7FFFu) mbits |= 1u << (part < 3 ? j - 20 * part : j - 60);
-      };
-      if (part < 3) {
-        int gg[2][4][5];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int p = 12 * c + 4 * part + b;
-          int y[2][6];
-#pragma unroll
-          for (int n = 0; n < 5; ++n) {
-            get(p, n, 5 * (4 * part + b) + n, y[0][n], y[1][n]);
-            xs[0] += y[0][n], xs[1] += y[1][n];
-          }
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            y[t][5] = 0;
-#pragma unroll
-            for (int k = 1; k <= 5; ++k) gg[t][b][k - 1] = y[t][k - 1] - 3 * y[t][k];
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int k = 0; k < 5; ++k) {
-            g[40 * t + 10 * part + 2 * k] = static_cast<int>((static_cast<uint32_t>(gg[t][0][k]) & 0xFFFFu) |
-                                                             (static_cast<uint32_t>(gg[t][1][k]) << 16));
-            g[40 * t + 10 * part + 2 * k + 1] = static_cast<int>((static_cast<uint32_t>(gg[t][2][k]) & 0xFFFFu) |
-                                                                 (static_cast<uint32_t>(gg[t][3][k]) << 16));
-          }
-      } else {
-        int y[2][5];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          get(48 + c, n, 60 + n, y[0][n], y[1][n]);
-          xs[0] += y[0][n], xs[1] += y[1][n];
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          y[t][4] = 0;
-#pragma unroll
-          for (int k = 1; k <= 4; ++k) g[40 * t + 30 + k - 1] = y[t][k - 1] - 3 * y[t][k];
-        }
-      }
-      g[34 + part] = xs[0];
-      g[40 + 34 + part] = xs[1];
-      g[80 + part] = static_cast<int>(mbits);
-    }
-  }
   __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
-    if (active) {
-      const uint32_t area = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + static_cast<uint32_t>(kCoefSB) * sbcol;
-      const uint32_t ga = area + 1024 + 384 * c_;
+    if (!active) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        uint32_t v[40];
-#pragma unroll
-        for (int i = 0; i < 10; ++i) {
-          const uint4 q = lds_v4(ga + 160 * t + 16 * i);
-          v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
-        }
-#pragma unroll
-        for (int w = 0; w < 3; ++w)
-#pragma unroll
-          for (int k = 0; k < 5; ++k) gw[t][w][k][0] = v[10 * w + 2 * k], gw[t][w][k][1] = v[10 * w + 2 * k + 1];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gq[t][k] = static_cast<int>(v[30 + k]);
-        xsum[t] = static_cast<int>(v[34]) + static_cast<int>(v[35]) + static_cast<int>(v[36]) + static_cast<int>(v[37]);
-      }
-      const uint4 mb = lds_v4(ga + 320);
-      // item masks: bits j in [0,20), [20,40), [40,60), [60,64)
-      res.rm0 = mb.x | (mb.y << 20);
-      res.rm1 = (mb.y >> 12) | (mb.z << 8) | (mb.w << 28);
-      res.ra = area + 512;
-      xf = 1.0f / X.e[sbcol];
-      xf_lo = xf * (1.0f / 8192.f);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-#pragma unroll
-        for (int w = 0; w < 3; ++w)
-#pragma unroll
-          for (int k = 0; k < 5; ++k) gw[t][w][k][0] = gw[t][w][k][1] = 0u;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gq[t][k] = 0;
-        xsum[t] = 0;
-      }
-      xf = xf_lo = 0.f;
-      res.clear();
+      for (int i = 0; i < 32; ++i) xr[i] = 0u;
+      return;
     }
+    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + static_cast<uint32_t>(kCoefSB * sbcol);
+    auto xv = [&](int p, int n) { return lds_u16(base + 2u * static_cast<uint32_t>(elem_of(p, n))); };
+#pragma unroll
+    for (int w = 0; w < 3; ++w)
+#pragma unroll
+      for (int n = 0; n < 5; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int p = 12 * c_ + 4 * w + h;
+          xr[10 * w + 2 * n + h] = xv(p, n) | (xv(p + 2, n) << 16);
+        }
+    xr[30] = xv(48 + c_, 0) | (xv(48 + c_, 2) << 16);
+    xr[31] = xv(48 + c_, 1) | (xv(48 + c_, 3) << 16);
   }
 
   struct Raw {
@@ -768,59 +642,33 @@ struct DecTQ10 {
   __device__ __forceinline__ float compute(const Raw& R_) const { return row(R_.b, 0); }
   // blk: shared-window address of the row's block (2-byte aligned: 54-byte blocks).
   __device__ __forceinline__ float row(uint32_t blk, uint32_t) const {
+    constexpr uint32_t kOne = 0x01000100u;  // 2^-16 in both f16 halves
     const uint32_t q = blk + 12 * c;
-    int acc = 0, acl = 0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < 3; ++w) {
       const uint32_t W = lds_u16(q + 4 * w) | (lds_u16(q + 4 * w + 2) << 16);
-      uint32_t pe = __byte_perm(W, 0u, 0x4240);  // bytes 0, 2 in 16-bit lanes
-      uint32_t po = __byte_perm(W, 0u, 0x4341);  // bytes 1, 3
+      uint32_t re = bytes02(W), ro = bytes13(W);
 #pragma unroll
-      for (int k = 0; k < 5; ++k) {
-        pe *= 3u;
-        po *= 3u;
-        const uint32_t F = __byte_perm(pe, po, 0x7351);  // F_k of bytes 0..3
-        acc = dp2a_lo_u(gw[0][w][k][0], F, acc);
-        acc = dp2a_hi_u(gw[0][w][k][1], F, acc);
-        acl = dp2a_lo_u(gw[1][w][k][0], F, acl);
-        acl = dp2a_hi_u(gw[1][w][k][1], F, acl);
+      for (int n = 0; n < 5; ++n) {
+        re *= 3u;
+        ro *= 3u;
+        const uint32_t te = hsub2_raw(re & 0x03000300u, kOne), to = hsub2_raw(ro & 0x03000300u, kOne);
+        if (n < 4) re &= 0x00FF00FFu, ro &= 0x00FF00FFu;
+        fma2h(acc[0], acc[1], xr[10 * w + 2 * n], te);
+        fma2h(acc[2], acc[3], xr[10 * w + 2 * n + 1], to);
       }
     }
-    uint32_t pq = lds_u8(blk + 48 + c);
+    const uint32_t b = lds_u8(blk + 48 + c);
+    uint32_t rq = b | (((9u * b) & 0xFFu) << 16);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      pq *= 3u;
-      const int f = static_cast<int>(pq >> 8);
-      acc += gq[0][k] * f;
-      acl += gq[1][k] * f;
+    for (int n = 0; n < 2; ++n) {
+      rq *= 3u;
+      const uint32_t tq = hsub2_raw(rq & 0x03000300u, kOne);
+      rq &= 0x00FF00FFu;
+      fma2h(acc[2 * n], acc[2 * n + 1], xr[30 + n], tq);
     }
-    const float d = h2f(lds_u16(blk + 52));
-    return d * fmaf(static_cast<float>(acc - xsum[0]), xf, static_cast<float>(acl - xsum[1]) * xf_lo);
-  }
-  __device__ __forceinline__ bool has_residual() const { return res.any(); }
-  // d times the sum of residual x element j times its weight t - 1, in fp32.
-  __device__ __forceinline__ float correction(uint32_t blk, uint32_t) const {
-    float acc = 0.f;
-    uint32_t m0 = res.rm0, m1 = res.rm1;
-    while (m0 | m1) {
-      int j;
-      if (m0) {
-        j = __ffs(m0) - 1;
-        m0 &= m0 - 1u;
-      } else {
-        j = 31 + __ffs(m1);
-        m1 &= m1 - 1u;
-      }
-      const bool qh = j >= 60;
-      const int p = qh ? 48 + c : 12 * c + j / 5;
-      const int n = qh ? j - 60 : j % 5;
-      const uint32_t b = lds_u8(blk + p);
-      uint32_t pw = 1u;
-      for (int i = 0; i < n; ++i) pw *= 3u;
-      const int t = static_cast<int>((3u * pw * b) >> 8) - 3 * static_cast<int>((pw * b) >> 8);
-      acc = fmaf(h2f(lds_u16(res.ra + 2u * elem_of(p, n))), static_cast<float>(t - 1), acc);
-    }
-    return h2f(lds_u16(blk + 52)) * acc;
+    return h2f(lds_u16(blk + 52)) * (((acc[0] + acc[1]) + (acc[2] + acc[3])) * 65536.f);
   }
 };
 

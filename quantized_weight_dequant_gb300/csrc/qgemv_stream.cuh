@@ -17,10 +17,10 @@
 //    bytes and dropped; lanes past a short last K-column are zeroed.
 //  * The Wk partial sums of a row are added in a fixed order in shared memory at the end,
 //    so results are bitwise reproducible.
-//  * x is staged once per CTA in shared memory, converted there to the decoders' form
-//    (exact fp16 pairs for the integer-code formats, scaled f16 for NVFP4, integer
-//    collapse coefficients for TQ1_0), then copied by each lane to registers.  Elements
-//    the staged form does not hold exactly are corrected per lane from their residuals.
+//  * x is staged once per CTA in shared memory, in the decoders' form (fp16 pairs for the
+//    integer-code formats and TQ1_0, scaled f16 for NVFP4), then copied by each lane to
+//    registers.  NVFP4 elements the scaled form does not hold exactly are corrected per
+//    lane from their residuals.
 //  * Under programmatic dependent launch the first weight stages are requested before the
 //    wait for the previous kernel (weights are not written by it); x is read after it.
 //  * The body is shared by the single-matrix kernel (fp32 row sums stored as they are) and

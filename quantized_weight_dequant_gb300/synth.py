@@ -163,6 +163,10 @@ LAYER_SHAPES = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4
 LAYER_MIXED = {"q": Q4_K, "k": Q5_K, "v": Q6_K, "o": Q8_0, "gate": Q4_K, "up": Q4_K, "down": Q6_K}
 SHAPE_SETS["layer"] = [(f"layer_{p}_{FORMAT_NAMES[LAYER_MIXED[p]]}_{n}x{k}", LAYER_MIXED[p], n, k)
                        for p, n, k in LAYER_SHAPES]
+# The same layer with every projection in every integer-code format (7 x 4 GEMVs).
+LAYER_FORMATS = (Q4_K, Q5_K, Q6_K, Q8_0)
+SHAPE_SETS["layer_every_format"] = [(f"layer_{p}_{FORMAT_NAMES[f]}_{n}x{k}", f, n, k)
+                                    for p, n, k in LAYER_SHAPES for f in LAYER_FORMATS]
 
 
 def shape_seed(set_name: str, shape_index: int) -> int:

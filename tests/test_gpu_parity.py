@@ -115,9 +115,9 @@ def test_ring_shapes_match_oracle(h, depth, rows):
 
 def _shape_cases():
     out = []
-    for sname in ("q4k_llama8b_decode", "nvfp4_llama8b", "tq1_0", "layer"):
+    for sname in ("q4k_llama8b_decode", "nvfp4_llama8b", "tq1_0", "layer", "layer_every_format"):
         for si, (name, fmt, N, K) in enumerate(synth.SHAPE_SETS[sname]):
-            out.append(pytest.param(sname, si, fmt, N, K, id=name))
+            out.append(pytest.param(sname, si, fmt, N, K, id=f"{sname}:{name}"))
     return out
 
 
