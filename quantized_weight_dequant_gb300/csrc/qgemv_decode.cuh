@@ -80,14 +80,19 @@ __device__ __forceinline__ uint32_t bytes02(uint32_t w) { return __byte_perm(w, 
 __device__ __forceinline__ uint32_t bytes13(uint32_t w) { return __byte_perm(w, 0u, 0x4341); }
 
 // ------------------------------------------------------------------- activation staging
-// The CTA's copy of x in shared memory: q[K] 16-bit values, e[K/32] one float per 32-element
-// chunk, g: the decoder's per-superblock area (kCoefSB bytes each), for decoders that have
-// one.
+// The CTA's copy of x in shared memory: q: 16-bit values, 16 bytes of padding after every 64
+// (so the 64-element pieces that the lanes of a quarter-warp copy to registers start on
+// different banks), e[K/32] one float per 32-element chunk, g: the decoder's per-superblock
+// area (kCoefSB bytes each), for decoders that have one.
 struct XStage {
   uint16_t* q;
   float* e;
   int* g;
 };
+// 16-byte slot of staged piece i (elements 8i .. 8i+7) in q, and the first value of the
+// 32-element chunk that starts at element k (a multiple of 32).
+__device__ __forceinline__ int xq_slot(int i) { return i + (i >> 3); }
+__device__ __forceinline__ const uint16_t* xq_at(const uint16_t* q, int k) { return q + k + 8 * (k >> 6); }
 
 // d = c + a.h0 * b.b0 + a.h1 * b.b1 (lo) / a.h0 * b.b2 + a.h1 * b.b3 (hi); a two int16,
 // b four unsigned bytes.
@@ -148,7 +153,7 @@ __device__ __forceinline__ uint32_t chunk_max_mag(const uint4& v) {
 // in fp32, in a fixed order) * 2^-24, for the group-minimum term.
 template <bool SUMS>
 __device__ __forceinline__ void flt_stage_piece(uint4 v, int i, const XStage& X) {
-  reinterpret_cast<uint4*>(X.q)[i] =
+  reinterpret_cast<uint4*>(X.q)[xq_slot(i)] =
       make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632), __byte_perm(v.z, v.w, 0x5410),
                  __byte_perm(v.z, v.w, 0x7632));
   if constexpr (SUMS) {
@@ -172,8 +177,8 @@ struct FltX {
   __device__ __forceinline__ void load(const XStage& X, int k0, int k1, bool active) {
     if (active) {
       uint32_t a[16], b[16];
-      ld_chunk(X.q + k0, a);
-      ld_chunk(X.q + k1, b);
+      ld_chunk(xq_at(X.q, k0), a);
+      ld_chunk(xq_at(X.q, k1), b);
 #pragma unroll
       for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
     } else {
@@ -488,7 +493,7 @@ struct DecNVFP4 {
       mask |= (d1 != 0.f ? 1u : 0u) << (2 * k + 1);
       w[k] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    reinterpret_cast<uint4*>(X.q)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(X.q)[xq_slot(i)] = make_uint4(w[0], w[1], w[2], w[3]);
     if ((i & 3) == 0) X.e[i >> 2] = inv;
     uint8_t* area = reinterpret_cast<uint8_t*>(X.g) + (i >> 5) * kCoefSB;
     reinterpret_cast<uint4*>(area)[i & 31] = make_uint4(r[0], r[1], r[2], r[3]);
@@ -499,8 +504,8 @@ struct DecNVFP4 {
     const int k0 = 256 * sbcol + 64 * c_;
     if (active) {
       uint32_t a[16], b[16];
-      ld_chunk(X.q + k0, a);
-      ld_chunk(X.q + k0 + 32, b);
+      ld_chunk(xq_at(X.q, k0), a);
+      ld_chunk(xq_at(X.q, k0 + 32), b);
 #pragma unroll
       for (int i = 0; i < 16; ++i) xr[i] = a[i], xr[16 + i] = b[i];
       const uint32_t ea = static_cast<uint32_t>(__cvta_generic_to_shared(X.e));

@@ -112,9 +112,9 @@ __host__ __device__ constexpr int slice_bytes() {
   return 8 * Dec::kSB + 8 * Dec::kSB2;
 }
 
-// Shared memory: [rings: warps * D * R * slice][reduction buffer][x staging: q (2K bytes),
-// e (K/32 floats)][decoder area: coef_sb bytes per superblock of the staged x][never-
-// completing barrier], each part 16-byte aligned.
+// Shared memory: [rings: warps * D * R * slice][reduction buffer][x staging: q (2K bytes
+// and 16 bytes of padding per 64 values), e (K/32 floats)][decoder area: coef_sb bytes per
+// superblock of the staged x][never-completing barrier], each part 16-byte aligned.
 struct StreamSmem {
   size_t red, xq, xe, xc, bar, total;
 };
@@ -124,7 +124,7 @@ __host__ __device__ inline StreamSmem stream_smem(int warps, int D, int R, int s
   StreamSmem m;
   m.red = static_cast<size_t>(warps) * D * R * slice;
   m.xq = align16(m.red + (Wk > 1 ? static_cast<size_t>(red_rows) * Wk * 4 : 0));
-  m.xe = align16(m.xq + static_cast<size_t>(K) * 2);
+  m.xe = align16(m.xq + static_cast<size_t>(K) * 2 + static_cast<size_t>(K / 64) * 16);
   m.xc = align16(m.xe + static_cast<size_t>(K / 32) * 4);
   m.bar = align16(m.xc + static_cast<size_t>(K / 256) * coef_sb);
   m.total = m.bar + 16;
@@ -322,42 +322,45 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   };
   static_assert(J1 <= 5, "row slice of at most 160 16-byte chunks");
 
-  // Activations: thread t copies 16-byte pieces t, t + blockDim.x, ... of x to the staging
-  // buffer (coalesced), then converts the same pieces in place, so only its own copies need
-  // to have landed.  Without programmatic dependent launch the x copies are requested
-  // first, ahead of the weight stages, so they are not queued behind them.  With it, the
-  // weight stages are requested before the wait for the previous kernel (whose output x
-  // may be), and x after.  The piece count K / 8 is a multiple of 32, so every warp runs
-  // the same number of conversions (they shuffle within groups of four lanes).  These
-  // loops run once per launch and are kept rolled: straight-line start-up code is fetched
-  // while the weight stream already loads the memory system.
+  // Activations: thread t loads 16-byte pieces t, t + blockDim.x, ... of x (coalesced, four
+  // at a time in flight) and converts them into the staging buffer.  Without programmatic
+  // dependent launch the first loads are issued ahead of the weight stages, so they are not
+  // queued behind them.  With it, the weight stages are requested before the wait for the
+  // previous kernel (whose output x may be), and x after.  The piece count is a multiple of
+  // 32, so every warp runs the same number of conversions (they shuffle within groups of
+  // lanes) and the predicates below are warp-uniform.  These loops run once per launch and
+  // are kept rolled: straight-line start-up code is fetched while the weight stream already
+  // loads the memory system.
   // Pieces of the K-columns this CTA reads (32 per superblock, so whole warps drop out).
   const int pc0 = 256 * kc0, pc1 = 32 * min(a.nsb, 8 * kc1);
-  auto issue_x = [&]() {
+  const uint4* const xs = reinterpret_cast<const uint4*>(a.x) + pc0;
+  const int npc = pc1 - pc0, nt = static_cast<int>(blockDim.x), tid = static_cast<int>(threadIdx.x);
+  auto stage_x = [&](bool stages_after_first_loads) {
 #pragma unroll 1
-    for (int i = pc0 + threadIdx.x; i < pc1; i += blockDim.x)
-      cp_async16(smem_u32(X.q) + 16 * (i - pc0), reinterpret_cast<const uint4*>(a.x) + i);
-    cp_async_commit();
+    for (int i0 = 0; i0 < npc; i0 += 4 * nt) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * nt + tid < npc) v[u] = __ldcg(xs + i0 + u * nt + tid);
+      if (stages_after_first_loads && i0 == 0) {
+#pragma unroll 1
+        for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * nt + tid < npc) Dec::stage_piece(v[u], i0 + u * nt + tid, X);
+    }
   };
   if (a.pdl == 1) {
-    // x is read with plain loads straight into the conversion: a cp.async group for it would
-    // be committed after the weight stages and could only be waited for together with them.
 #pragma unroll 1
     for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
     pdl_wait();
     QG_TRACE(1);
-#pragma unroll 1
-    for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x)
-      Dec::stage_piece(__ldcg(reinterpret_cast<const uint4*>(a.x) + pc0 + i), i, X);
+    stage_x(false);
   } else {
     pdl_wait();  // at once without programmatic dependent launch
-    issue_x();
-#pragma unroll 1
-    for (int s = 0; s < D - 1; ++s) issue(s, ring_sa + s * STAGE);
-    cp_async_wait<D - 1>();
     QG_TRACE(1);
-#pragma unroll 1
-    for (int i = threadIdx.x; i < pc1 - pc0; i += blockDim.x) Dec::stage_piece(reinterpret_cast<const uint4*>(X.q)[i], i, X);
+    stage_x(true);
   }
   __syncthreads();
   QG_TRACE(2);
@@ -368,6 +371,7 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   Dec dec;
   dec.init(lane & 3);
   dec.load_x(X, 8 * (wk - kc0) + col, lane & 3, active);  // superblock index within the buffer
+  QG_TRACE(6);
 
   // Where row sums go: y (one K-column), the workspace (split mode) or the CTA's reduction
   // buffer (fused mode, stride Wk).
@@ -383,6 +387,7 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   float* optr = out + (lane / LPR) * ostride;
   for (int st = 0; st < nst; ++st) {
     issue(st + D - 1, is);
+    if (st == 0) QG_TRACE(7);
     cp_async_wait<D - 1>();
     __syncwarp();
     if (st == 0) QG_TRACE(3);
