@@ -284,12 +284,15 @@ bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool gene
   if (total_ranges > kMaxRanges || ws_need > static_cast<int64_t>(kWsFloats)) return false;
   if (total_grid > 0x7fffffff) return false;
   const int Kx = split ? static_cast<int>(std::min<int64_t>(K, 2048)) : static_cast<int>(K);
-  // Ring shape.  Defaults: 2 rows per stage, 4 stages; split launches (long K): 4 rows, 2
-  // stages; a one-CTA-per-SM launch of a two-per-SM layout: 4 rows, 3 stages.
-  const bool long_k = split && Wk > 1;
+  // Ring shape.  Defaults: 4 rows per stage, 2 stages (measured on the 28672 x 4096 decode
+  // shape: fewer stage turns per row than 2 rows x 4 stages for the same bytes in flight);
+  // a one-CTA-per-SM launch of a two-per-SM layout: 4 rows, 3 stages (split launches keep 2);
+  // one K-column (K <= 2048): 2 rows, 4 stages.
   const bool half = gps < cps;
-  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : (long_k || half ? 4 : 2);
-  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : (long_k ? 2 : half ? 3 : 4);
+  const bool one_col = Wk == 1 && !half;
+  const int Rdef = one_col ? 2 : 4, Ddef = one_col ? 4 : (half && !(split && Wk > 1)) ? 3 : 2;
+  int R = h.rows_per_stage > 0 ? (h.rows_per_stage >= 4 ? 4 : h.rows_per_stage >= 2 ? 2 : 1) : Rdef;
+  int D = h.ring_depth > 0 ? std::min(h.ring_depth, 4) : Ddef;
   const int Rmin = general ? 2 : 1;
   if (R < Rmin) R = Rmin;
   const size_t cap = static_cast<size_t>((228 * 1024) / cps - 1024);
