@@ -327,15 +327,19 @@ struct BatchQ5K {
 // ----------------------------------------------------------------------------- Q8_0
 // A superblock is 8 blocks of 34 bytes (d, then 32 int8 codes).  Lane t4 takes blocks 2 t4 and
 // 2 t4 + 1 (bytes [68 t4, 68 t4 + 68), read as 17 aligned words), one word of 4 codes per
-// k-step.  A = d * q rounded once to fp16 (the block scale differs between the lanes of a
-// k-step, so it cannot wait for the accumulator): a relative error of at most 2^-11 per
-// weight, a quarter of the GEMV bound.
+// k-step.  The block scale changes between the lanes of a k-step, so it cannot wait for the
+// accumulator: A = fp16(d' q), rounded once per weight (relative error at most 2^-11, a
+// quarter of the GEMV bound), with d' = d 2^sigma, sigma per row and superblock chosen from
+// the row's largest block scale so that every |d' q| < 2^15.  That keeps the operands out of
+// the fp16 subnormals (where rounding would be an absolute 2^-25, not a relative error) for
+// every block within 2^21 of the row's largest one; the superblock's sums are multiplied by
+// 2^-sigma in fp32.
 struct BatchQ80 {
   static constexpr int kSB = 272, kSB2 = 0;
   // one superblock per stage (two would not fit 16 warps x 2 stages), slots padded by 32 so
   // the word loads of the 8 rows g fall in different banks
   static constexpr int kStageSB = 1, kPad = 32;
-  static constexpr bool kMinTerm = false, kFolded = true, kBF16 = false, kWindow = false;
+  static constexpr bool kMinTerm = false, kFolded = false, kBF16 = false, kWindow = false;
 
   // elements 64 t4 + 4 s + (0..3): pairs (x0, x2) and (x1, x3), as bytes (b0, b2), (b1, b3)
   __device__ __forceinline__ static void chunk_slot(int e, int& step, int& t4, uint2& v, uint2 raw) {
@@ -352,8 +356,8 @@ struct BatchQ80 {
     uint32_t w[17];
 #pragma unroll
     for (int k = 0; k < 17; ++k) w[k] = lds_u32(base + 4 * k);
-    dA = __byte_perm(w[0], w[0], 0x1010);
-    dB = __byte_perm(w[8], w[8], 0x3232);
+    dA = w[0] & 0xFFFFu;
+    dB = w[8] >> 16;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       q[k] = __byte_perm(w[k], w[k + 1], 0x5432);
@@ -361,15 +365,34 @@ struct BatchQ80 {
     }
   }
 
+  // The row's scale 2^sigma from the largest |d| of its 8 blocks (the lane's two, then the
+  // four lanes t4 of the row), and the lane's two scaled block scales as fp16 pairs.
+  __device__ __forceinline__ static float row_scale(uint32_t dA, uint32_t dB, uint32_t& pA, uint32_t& pB) {
+    uint32_t m = max(dA & 0x7FFFu, dB & 0x7FFFu);
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    // |d| < 2^(E + 1) for the largest: 2^sigma = 2^(7 - E) puts it in [2^7, 2^8), |d' q| < 2^15
+    const int E = m ? static_cast<int>((__float_as_uint(h2f(m)) >> 23) & 0xFFu) - 127 : 0;
+    const float sc = p2(7 - E);
+    const uint32_t a = __half_as_ushort(__float2half_rn(h2f(dA) * sc));
+    const uint32_t b = __half_as_ushort(__float2half_rn(h2f(dB) * sc));
+    pA = a | (a << 16);
+    pB = b | (b << 16);
+    return p2(E - 7);
+  }
+
   __device__ __forceinline__ static void superblock(uint32_t rg, uint32_t r8, int c, int t4, uint32_t xa, uint32_t,
-                                                    uint32_t magic, float (&dq)[2][4]) {
+                                                    uint32_t magic, float (&y)[4]) {
     uint32_t qg[16], q8[16], dAg, dBg, dA8, dB8;
     lane_blocks(rg + kSB * c + 68 * t4, qg, dAg, dBg);
     lane_blocks(r8 + kSB * c + 68 * t4, q8, dA8, dB8);
+    uint32_t pAg, pBg, pA8, pB8;
+    const float ig = row_scale(dAg, dBg, pAg, pBg), i8 = row_scale(dA8, dB8, pA8, pB8);
     const uint32_t off = 0x64806480u;  // fp16 (1152, 1152) = 1024 + 128
+    float dq[2][4] = {};
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
-      const uint32_t dg = s < 8 ? dAg : dBg, d8 = s < 8 ? dA8 : dB8;
+      const uint32_t dg = s < 8 ? pAg : pBg, d8 = s < 8 ? pA8 : pB8;
       const uint32_t ug = qg[s] ^ 0x80808080u, u8 = q8[s] ^ 0x80808080u;  // q + 128 per byte
       const uint2 xs_ = lds_v2(xa + s * 256);
       mma16816(dq[s & 1], hmul2_u(hsub2_u(and_or<0x00FF00FFu>(ug, magic), off), dg),
@@ -377,6 +400,10 @@ struct BatchQ80 {
                hmul2_u(hsub2_u(and_or<0x00FF00FFu>(ug >> 8, magic), off), dg),
                hmul2_u(hsub2_u(and_or<0x00FF00FFu>(u8 >> 8, magic), off), d8), xs_.x, xs_.y);
     }
+    y[0] = fmaf(dq[0][0] + dq[1][0], ig, y[0]);
+    y[1] = fmaf(dq[0][1] + dq[1][1], ig, y[1]);
+    y[2] = fmaf(dq[0][2] + dq[1][2], i8, y[2]);
+    y[3] = fmaf(dq[0][3] + dq[1][3], i8, y[3]);
   }
 };
 

@@ -180,3 +180,33 @@ def test_batch_full_size_sampled_rows(h, fmt, N, K, M):
         qgemv.set_option(h, qgemv.OPT_PDL, 0)
     _check(y.cpu().numpy(), X, fmt, W, N, K, rows=sample_rows(N, 48, seed=N), what="full size")
     assert qgemv.check_error(h) == qgemv.OK
+
+
+def _q80_small_scales(N, K, seed, lo, hi, codes=None):
+    """Q8_0 weights whose block scales d are drawn log-uniformly from [lo, hi] (fp16, many of
+    them fp16 subnormals below 6.1e-5) and, with `codes`, whose int8 codes all lie in that set:
+    small codes against all-positive activations make rounding errors of the operand add up
+    instead of cancelling."""
+    W = synth.make_weights(synth.Q8_0, N, K, seed).reshape(N, K // 32, 34).copy()
+    rng = np.random.default_rng(seed)
+    d = np.exp(rng.uniform(np.log(lo), np.log(hi), size=W.shape[:2])).astype(np.float16)
+    W[:, :, 0:2] = d.view(np.uint8).reshape(N, K // 32, 2)
+    if codes is not None:
+        W[:, :, 2:] = rng.choice(np.array(codes, dtype=np.int8), size=(N, K // 32, 32)).view(np.uint8)
+    return W.reshape(-1)
+
+
+@pytest.mark.parametrize("lo,hi,codes", [(1e-7, 3e-6, [1, 2, 3]), (2e-8, 1e-5, None), (1e-6, 1e-3, [1, -1, 2]),
+                                         (6e-8, 6e-8, [1])])
+def test_q80_batch_tiny_block_scales(h, lo, hi, codes):
+    """Block scales in and around the fp16 subnormals: the operand d q is scaled per row and
+    superblock into fp16's normal range, so its rounding stays relative (at most 2^-11 of each
+    weight) and every output stays inside the GEMV bound, where a subnormal operand's absolute
+    rounding would not."""
+    N, K = 96, 4096
+    W = _q80_small_scales(N, K, seed=71, lo=lo, hi=hi, codes=codes)
+    Wd, _ = dev_bytes(W)
+    for M in (2, 5):
+        X = np.abs(_xs(synth.Q8_0, M, K, seed=73).view(np.float16)).astype(np.float16).view(np.uint16)
+        Y = _run(h, synth.Q8_0, X, Wd, N, K)
+        _check(Y, X, synth.Q8_0, W, N, K, what=f"Q8_0 d in [{lo}, {hi}] M={M}")
