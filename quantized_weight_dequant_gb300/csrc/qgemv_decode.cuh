@@ -199,6 +199,7 @@ struct FltX {
 // mixed-precision FMAs (a 6-bit value placed as an f16 subnormal gives d*s*2^-24 exactly).
 struct DecQ4K : FltX {
   static constexpr int kSB = 144, kSB2 = 0;
+  static constexpr float kOut = kTwo48;  // unit of compute()'s results
   static constexpr int kCoefSB = 0;
   static constexpr bool kPrep = false, kResidual = false;
   int c;
@@ -220,15 +221,11 @@ struct DecQ4K : FltX {
     m2 = (c < 2) ? 0u : 0x00300030u;
     shm = (c < 2) ? 0u : 4u;
   }
-  __device__ __forceinline__ void load_x_plain(const XStage& X, int sbcol, int c_, bool active) {
+  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
     const int k0 = 256 * sbcol + 64 * c_;
     load(X, k0, k0 + 32, active);
     xs0 = active ? X.e[k0 >> 5] : 0.f;
     xs1 = active ? X.e[(k0 >> 5) + 1] : 0.f;
-  }
-  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
-    load_x_plain(X, sbcol, c_, active);
-    xs1 *= 16.f;  // the high-nibble sums come out 16 times too large: see compute()
   }
   // d*s_lo, d*s_hi, dmin*m_lo, dmin*m_hi (times 2^-24) from the block header.
   __device__ __forceinline__ void scales(const uint4 h, float& ds_lo, float& ds_hi, float& dm_lo, float& dm_hi) const {
@@ -237,13 +234,14 @@ struct DecQ4K : FltX {
     mul1x2h(ds_lo, ds_hi, h.x, s2);
     mul1x2h(dm_lo, dm_hi, h.x >> 16, m2v);
   }
-  // a_lo = sum(x q) 2^-24 (group 2c), a_hi = sum(x q) 2^-24 times H (group 2c+1); the
-  // result in true units: (ds a - dm xs) carries 2^-48, and the high group 16 / H more.
-  __device__ __forceinline__ float combine(float a_lo, float a_hi, float ds_lo, float ds_hi, float dm_lo, float dm_hi,
-                                           float hi_scale) const {
-    const float t0 = fmaf(ds_lo, a_lo, -dm_lo * xs0);
-    const float t1 = fmaf(ds_hi, a_hi, -dm_hi * xs1);
-    return fmaf(t0, kTwo48, t1 * hi_scale);
+  // a_lo = sum(x q) 2^-24 (group 2c), a_hi the same for group 2c+1 (16 times too large with
+  // HI16: high nibbles left in place).  Returns the piece's sum in units of 2^-48 (kOut):
+  // ds_lo a_lo + ds_hi a_hi - (dm_lo xs0 + dm_hi xs1).
+  template <bool HI16>
+  __device__ __forceinline__ float combine(float a_lo, float a_hi, float ds_lo, float ds_hi, float dm_lo,
+                                           float dm_hi) const {
+    const float m = fmaf(dm_lo, xs0, dm_hi * xs1);
+    return fmaf(ds_lo, a_lo, fmaf(HI16 ? ds_hi * 0.0625f : ds_hi, a_hi, -m));
   }
 
   // blk: shared-window address of the row's superblock slice (16-byte aligned).
@@ -259,19 +257,18 @@ struct DecQ4K : FltX {
   __device__ __forceinline__ float compute(const Raw& R_) const {
     const uint4 h = R_.h, q0 = R_.q0, q1 = R_.q1;
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+    float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f};  // the rows of a stage give the other chains
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t w8 = w[u] >> 8;
-      const int o = 2 * (u & 1);
-      fma2h(a[o], a[o + 1], xr[2 * u], w[u] & 0x000F000Fu);      // elements t, t+2
-      fma2h(a[o], a[o + 1], xr[2 * u + 1], w8 & 0x000F000Fu);    // t+1, t+3
-      fma2h(b[o], b[o + 1], xr[16 + 2 * u], w[u] & 0x00F000F0u);  // 32+t, 34+t (16 q)
-      fma2h(b[o], b[o + 1], xr[16 + 2 * u + 1], w8 & 0x00F000F0u);
+      fma2h(a[0], a[1], xr[2 * u], w[u] & 0x000F000Fu);      // elements t, t+2
+      fma2h(a[0], a[1], xr[2 * u + 1], w8 & 0x000F000Fu);    // t+1, t+3
+      fma2h(b[0], b[1], xr[16 + 2 * u], w[u] & 0x00F000F0u);  // 32+t, 34+t (16 q)
+      fma2h(b[0], b[1], xr[16 + 2 * u + 1], w8 & 0x00F000F0u);
     }
     float ds_lo, ds_hi, dm_lo, dm_hi;
     scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
-    return combine((a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3]), ds_lo, ds_hi, dm_lo, dm_hi, kTwo44);
+    return combine<true>(a[0] + a[1], b[0] + b[1], ds_lo, ds_hi, dm_lo, dm_hi);
   }
 };
 
@@ -284,10 +281,6 @@ struct DecQ5K : DecQ4K {
   static constexpr int kSB = 176, kSB2 = 0;
   static constexpr int kCoefSB = 0;
   uint32_t rl, rh;  // rotate amounts bringing bit 2c / 2c+1 of each byte to bit 4
-
-  __device__ __forceinline__ void load_x(const XStage& X, int sbcol, int c_, bool active) {
-    load_x_plain(X, sbcol, c_, active);
-  }
 
   __device__ __forceinline__ void init(int c_) {
     DecQ4K::init(c_);
@@ -308,20 +301,19 @@ struct DecQ5K : DecQ4K {
     const uint4 qb = lds_v4(blk + 64 + 32 * c);
     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+    float a[2] = {0.f, 0.f}, b[2] = {0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t L = (w[u] & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rl) & 0x10101010u);
       const uint32_t H = ((w[u] >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(e[u], e[u], rh) & 0x10101010u);
-      const int o = 2 * (u & 1);
-      fma2h(a[o], a[o + 1], xr[2 * u], bytes02(L));
-      fma2h(a[o], a[o + 1], xr[2 * u + 1], bytes13(L));
-      fma2h(b[o], b[o + 1], xr[16 + 2 * u], bytes02(H));
-      fma2h(b[o], b[o + 1], xr[16 + 2 * u + 1], bytes13(H));
+      fma2h(a[0], a[1], xr[2 * u], bytes02(L));
+      fma2h(a[0], a[1], xr[2 * u + 1], bytes13(L));
+      fma2h(b[0], b[1], xr[16 + 2 * u], bytes02(H));
+      fma2h(b[0], b[1], xr[16 + 2 * u + 1], bytes13(H));
     }
     float ds_lo, ds_hi, dm_lo, dm_hi;
     scales(h, ds_lo, ds_hi, dm_lo, dm_hi);
-    return combine((a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3]), ds_lo, ds_hi, dm_lo, dm_hi, kTwo48);
+    return combine<false>(a[0] + a[1], b[0] + b[1], ds_lo, ds_hi, dm_lo, dm_hi);
   }
 };
 
@@ -334,6 +326,7 @@ struct DecQ5K : DecQ4K {
 // bytes (2-byte aligned), so quant words are read with a byte permute.
 struct DecQ6K : FltX {
   static constexpr int kSB = 210, kSB2 = 0;
+  static constexpr float kOut = kTwo24;
   static constexpr int kCoefSB = 0;
   static constexpr bool kPrep = false, kResidual = false;
   int c;
@@ -378,7 +371,7 @@ struct DecQ6K : FltX {
       fma2h(acc[2 + g][0], acc[2 + g][1], xr[16 + 2 * u + 1], hsub2_raw(bytes13(hi6), k32));
     }
     const uint32_t sc = blk + 192 + 8 * H + 2 * rr;
-    const float d = h2f(lds_u16(blk + 208)) * kTwo24;
+    const float d = h2f(lds_u16(blk + 208));
     const float r0 = fmaf(static_cast<float>(lds_s8(sc)), acc[0][0] + acc[0][1],
                           static_cast<float>(lds_s8(sc + 1)) * (acc[1][0] + acc[1][1]));
     const float r1 = fmaf(static_cast<float>(lds_s8(sc + 4)), acc[2][0] + acc[2][1],
@@ -393,6 +386,7 @@ struct DecQ6K : FltX {
 // an f16 lane as the subnormal (b + 128) 2^-24 and made b 2^-24 by one exact subtraction.
 struct DecQ80 : FltX {
   static constexpr int kSB = 272, kSB2 = 0;
+  static constexpr float kOut = kTwo24;
   static constexpr int kCoefSB = 0;
   static constexpr bool kPrep = false, kResidual = false;
   int c;
@@ -426,7 +420,7 @@ struct DecQ80 : FltX {
       }
       r[e] = h2f(lds_u16(blk)) * ((a[0] + a[1]) + (a[2] + a[3]));
     }
-    return (r[0] + r[1]) * kTwo24;
+    return r[0] + r[1];
   }
 };
 
@@ -468,6 +462,7 @@ struct Residual {
 // byte per 8 elements.
 struct DecNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
+  static constexpr float kOut = 1.f;
   static constexpr int kCoefSB = 256 * 2 + 32;
   static constexpr bool kPrep = false, kResidual = true;
   uint32_t xr[32];
@@ -605,6 +600,7 @@ struct DecNVFP4 {
 // word w, registers 30 / 31 the qh digits (0, 2) / (1, 3).
 struct DecTQ10 : FltX {
   static constexpr int kSB = 54, kSB2 = 0;
+  static constexpr float kOut = 65536.f;
   static constexpr int kCoefSB = 528;
   static constexpr bool kPrep = false, kResidual = false;
   int c;
@@ -673,7 +669,7 @@ struct DecTQ10 : FltX {
       rq &= 0x00FF00FFu;
       fma2h(acc[2 * n], acc[2 * n + 1], xr[30 + n], tq);
     }
-    return h2f(lds_u16(blk + 52)) * (((acc[0] + acc[1]) + (acc[2] + acc[3])) * 65536.f);
+    return h2f(lds_u16(blk + 52)) * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
   }
 };
 

@@ -410,7 +410,7 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
     cs = (cs + STAGE == ring_end) ? ring_sa : cs + STAGE;
 #pragma unroll
     for (int r = 0; r < R; ++r) v[r] = active ? v[r] : 0.f;
-    const float sum = reduce_rows<R>(v, lane);
+    const float sum = reduce_rows<R>(v, lane) * Dec::kOut;  // the decoder's unit, once per row
     if (pair) {  // virtual row 2j (gate) or 2j + 1 (up) of the warp's output j
       const int q = st * R + lane / LPR;
       if (writer && q < nrows) out[(q < np ? 2 * q : 2 * (q - np) + 1) * ostride] = sum;
