@@ -142,8 +142,7 @@ int qgemv_group_size(qgemv_format_t fmt);
  *                             cp.async.wait_group, which the hardware completes.)
  *   QGEMV_OPT_PDL             1 launches the streaming kernels with programmatic dependent
  *                             launch: they may start while the previous kernel on the stream
- *                             is still running, and a launch that leaves room on each SM
- *                             (see QGEMV_OPT_GRID_PER_SM) requests its first weight stages
+ *                             is still running, and they request their first weight stages
  *                             before waiting for it; activations are read only after it
  *                             completes.  packed_W must therefore not be written by the kernel
  *                             launched just before.  0 (default) launches them normally.

@@ -347,11 +347,11 @@ bool plan_stream(const Handle& h, const Problem* ps, int n, int64_t K, bool gene
     a.err = h.err;
     a.spin_ns = h.spin_ns;
     a.test_stall = i == 0 ? h.test_stall : 0;
-    // Under programmatic dependent launch, a launch that leaves room on each SM for the next
-    // one requests its first weight stages before waiting for the previous kernel (kernel
-    // mode 1); one that fills the SMs cannot overlap much, and takes x first (mode 2), so x is
-    // not queued behind its own weight stages.
-    a.pdl = !h.pdl ? 0 : (gps < cps ? 1 : 2);
+    // Under programmatic dependent launch every launch requests its first weight stages before
+    // waiting for the previous kernel (kernel mode 1; measured faster than taking x first, mode
+    // 2, also on launches that fill the SMs: CTAs that start as the previous kernel's leave
+    // their SM have their first weights in flight while the rest of it finishes).
+    a.pdl = !h.pdl ? 0 : 1;
     a.split = split ? 1 : 0;
     a.ws = h.ws + ws_off;
     a.cnt = h.cnt + rng;
