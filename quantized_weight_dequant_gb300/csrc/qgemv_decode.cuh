@@ -605,12 +605,6 @@ struct DecTQ10 : FltX {
   static constexpr bool kPrep = false, kResidual = false;
   int c;
 
-  // Element of the superblock that digit n of byte p weighs (p < 48: qs, else qh).
-  __device__ __forceinline__ static int elem_of(int p, int n) {
-    if (p < 32) return 32 * n + p;
-    if (p < 48) return 160 + 16 * n + (p - 32);
-    return 240 + 4 * n + (p - 48);
-  }
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {
     *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(X.g) + kCoefSB * (i >> 5) + 16 * (i & 31)) = v;
   }
@@ -622,18 +616,25 @@ struct DecTQ10 : FltX {
       return;
     }
     const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(X.g)) + static_cast<uint32_t>(kCoefSB * sbcol);
-    auto xv = [&](int p, int n) { return lds_u16(base + 2u * static_cast<uint32_t>(elem_of(p, n))); };
+    // Word w of the piece is bytes p..p+3, p = 12 c + 4 w (a multiple of 4, all in one of the
+    // two qs runs), whose digit-n elements are four consecutive staged values: one 8-byte load
+    // and two byte permutes give the pairs (bytes 0, 2) and (1, 3).
 #pragma unroll
-    for (int w = 0; w < 3; ++w)
+    for (int w = 0; w < 3; ++w) {
+      const int p = 12 * c_ + 4 * w;
+      const bool first = p < 32;
 #pragma unroll
-      for (int n = 0; n < 5; ++n)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int p = 12 * c_ + 4 * w + h;
-          xr[10 * w + 2 * n + h] = xv(p, n) | (xv(p + 2, n) << 16);
-        }
-    xr[30] = xv(48 + c_, 0) | (xv(48 + c_, 2) << 16);
-    xr[31] = xv(48 + c_, 1) | (xv(48 + c_, 3) << 16);
+      for (int n = 0; n < 5; ++n) {
+        const int e = first ? 32 * n + p : 160 + 16 * n + (p - 32);
+        uint32_t lo, hi;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(base + 2u * static_cast<uint32_t>(e)));
+        xr[10 * w + 2 * n] = __byte_perm(lo, hi, 0x5410);      // elements p, p + 2
+        xr[10 * w + 2 * n + 1] = __byte_perm(lo, hi, 0x7632);  // p + 1, p + 3
+      }
+    }
+    auto xv = [&](int n) { return lds_u16(base + 2u * static_cast<uint32_t>(240 + 4 * n + c_)); };
+    xr[30] = xv(0) | (xv(2) << 16);
+    xr[31] = xv(1) | (xv(3) << 16);
   }
 
   struct Raw {
