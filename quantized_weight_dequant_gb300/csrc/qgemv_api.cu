@@ -197,7 +197,7 @@ void rowwarp_plan(const Handle& h, int64_t N, Plan& pl) {
 }
 
 int slice_of(int f) { return 8 * sb_bytes(f) + 8 * sb_bytes2(f); }
-// Decoder area bytes per staged superblock (TQ1_0's collapse coefficients and residuals,
+// Decoder area bytes per staged superblock (TQ1_0's x in its own per-superblock slots,
 // NVFP4's residuals); must equal the decoder's kCoefSB.
 int coef_of(int f) { return f == F_TQ10 ? DecTQ10::kCoefSB : f == F_NVFP4 ? DecNVFP4::kCoefSB : 0; }
 

@@ -201,7 +201,7 @@ struct DecQ4K : FltX {
   static constexpr int kSB = 144, kSB2 = 0;
   static constexpr float kOut = kTwo48;  // unit of compute()'s results
   static constexpr int kCoefSB = 0;
-  static constexpr bool kPrep = false, kResidual = false;
+  static constexpr bool kResidual = false;
   int c;
   uint32_t sel_s, sel_h, m1, m2, shm;
   uint32_t qoff;   // byte offset of this lane's quants in a block
@@ -328,7 +328,7 @@ struct DecQ6K : FltX {
   static constexpr int kSB = 210, kSB2 = 0;
   static constexpr float kOut = kTwo24;
   static constexpr int kCoefSB = 0;
-  static constexpr bool kPrep = false, kResidual = false;
+  static constexpr bool kResidual = false;
   int c;
   uint32_t rlo, rhi;  // rotate amounts bringing qh bits 2rr / 2rr+4 of each byte to bit 4
 
@@ -388,7 +388,7 @@ struct DecQ80 : FltX {
   static constexpr int kSB = 272, kSB2 = 0;
   static constexpr float kOut = kTwo24;
   static constexpr int kCoefSB = 0;
-  static constexpr bool kPrep = false, kResidual = false;
+  static constexpr bool kResidual = false;
   int c;
 
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) { flt_stage_piece<false>(v, i, X); }
@@ -464,7 +464,7 @@ struct DecNVFP4 {
   static constexpr int kSB = 128, kSB2 = 16;
   static constexpr float kOut = 1.f;
   static constexpr int kCoefSB = 256 * 2 + 32;
-  static constexpr bool kPrep = false, kResidual = true;
+  static constexpr bool kResidual = true;
   uint32_t xr[32];
   float xf0, xf1;
   int c;
@@ -602,7 +602,7 @@ struct DecTQ10 : FltX {
   static constexpr int kSB = 54, kSB2 = 0;
   static constexpr float kOut = 65536.f;
   static constexpr int kCoefSB = 528;
-  static constexpr bool kPrep = false, kResidual = false;
+  static constexpr bool kResidual = false;
   int c;
 
   __device__ __forceinline__ static void stage_piece(uint4 v, int i, const XStage& X) {

@@ -364,10 +364,6 @@ __device__ __forceinline__ void stream_body(const StreamArgs& a, const int cta, 
   }
   __syncthreads();
   QG_TRACE(2);
-  if constexpr (Dec::kPrep) {  // per-CTA decoder coefficients of the staged x
-    Dec::prep(X, (pc1 - pc0) / 32, threadIdx.x, blockDim.x);
-    __syncthreads();
-  }
   Dec dec;
   dec.init(lane & 3);
   dec.load_x(X, 8 * (wk - kc0) + col, lane & 3, active);  // superblock index within the buffer

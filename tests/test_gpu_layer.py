@@ -100,9 +100,7 @@ def test_general_epilogue_matches_oracle(h, fmt, N, K):
                                      (synth.Q6_K, 40, 12288), (synth.TQ1_0, 200, 4096), (synth.TQ1_0, 70, 14336),
                                      (synth.TQ1_0, 9, 256)])
 def test_general_epilogue_with_unit_alpha_equals_run_bitwise(h, fmt, N, K):
-    """qgemv_run against the grouped kernel with out = 1 * r + 0: the same sums bit for bit.
-    For TQ1_0 this also sets the collapse coefficients prepared once per GEMV (qgemv_run)
-    against those each CTA of the grouped kernel prepares itself."""
+    """qgemv_run against the grouped kernel with out = 1 * r + 0: the same sums bit for bit."""
     _, Wd = _weights(fmt, N, K, seed=3 + fmt)
     xd = dev_x(synth.make_x(fmt, K, seed=3))
     y0 = torch.empty(N, dtype=torch.float32, device="cuda")
