@@ -614,25 +614,33 @@ def run_ours(args, gemvs, rank, world):
     step_bytes = sum(unit_bytes(gemvs, idx, sw, B) for _, idx, sw in units)
     stream = torch.cuda.Stream(device=dev)
 
-    def launch(ui, c, s):
-        """Launch unit ui on weight copy c."""
+    # A second set of x / y buffers, for the end-to-end run's double buffering.
+    xall2 = xall.clone()
+    xs2 = {k: xall2[xoff[k]:xoff[k] + v.numel()].view(v.shape) for k, v in xs.items()}
+    yall2 = torch.empty_like(yall)
+    ys2 = [None if y is None else yall2[o:o + y.numel()].view(y.shape) for o, y in zip(yoff, ys)]
+    bufs = [(xs, ys), (xs2, ys2)]
+
+    def launch(ui, c, s, bs=0):
+        """Launch unit ui on weight copy c, with buffer set bs."""
         label, idx, sw = units[ui]
         _, fmt, N, K, xk = gemvs[idx[0]]
-        x = xs[(xk, K, fmt)]
+        xv, yv = bufs[bs]
+        x = xv[(xk, K, fmt)]
         if label not in grouped and B > 1:
-            qgemv.run_batch(h, fmt, x, B, Ws[idx[0]][c], N, K, ys[idx[0]], stream=s)
+            qgemv.run_batch(h, fmt, x, B, Ws[idx[0]][c], N, K, yv[idx[0]], stream=s)
         elif label not in grouped:
-            qgemv.run(h, fmt, x, Ws[idx[0]][c], N, K, ys[idx[0]], stream=s)
+            qgemv.run(h, fmt, x, Ws[idx[0]][c], N, K, yv[idx[0]], stream=s)
         elif sw:
-            qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[idx[0]][c], N, ys[idx[0]], packed_W_up=Ws[idx[1]][c],
+            qgemv.run_group(h, x, K, [qgemv.problem(fmt, Ws[idx[0]][c], N, yv[idx[0]], packed_W_up=Ws[idx[1]][c],
                                                     swiglu=True)], stream=s)
         else:
-            qgemv.run_group(h, x, K, [qgemv.problem(gemvs[i][1], Ws[i][c], gemvs[i][2], ys[i]) for i in idx], stream=s)
+            qgemv.run_group(h, x, K, [qgemv.problem(gemvs[i][1], Ws[i][c], gemvs[i][2], yv[i]) for i in idx], stream=s)
 
-    def step(i, s):
+    def step(i, s, bs=0):
         c = i % copies
         for ui in range(len(units)):
-            launch(ui, c, s)
+            launch(ui, c, s, bs)
 
     # sanity: one step, checked for errors, before anything is captured
     with torch.cuda.stream(stream):
@@ -764,31 +772,60 @@ def run_ours(args, gemvs, rank, world):
 
     # End to end through the public API: the step's packed x from pinned host memory to the
     # device (one copy), one qgemv call per launch unit, the packed outputs back (one copy).
+    # Steps are pipelined as a serving loop runs independent requests: step i's input copy and
+    # step i - 1's result copy run on copy streams while step i - 1 / i compute, with two
+    # device buffer sets (step i uses set i % 2).  Events keep each buffer safe: a step's
+    # compute waits for its input copy and for the result copy that last read its y buffer;
+    # an input copy waits for the compute that last read its x buffer.
     e2e_steps = min(args.steps, 2000)
     hx = torch.empty(xall.shape, dtype=torch.int16).pin_memory()
     hx.copy_(xall.cpu())
-    hy = torch.empty(yall.shape, dtype=torch.float32).pin_memory()
+    hys = [torch.empty(yall.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    xalls, yalls = [xall, xall2], [yall, yall2]
     h2d = 2 * xall.numel()
     d2h = 4 * yall.numel()
-    def e2e_step(i):
-        xall.copy_(hx, non_blocking=True)
-        step(i, stream)
-        hy.copy_(yall, non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_steps_run(n):
+        """n pipelined steps on `stream` (compute), s_in and s_out (copies); joined at the end."""
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        computed = [None, None]  # event: the last compute that used buffer set p
+        copied_out = [None, None]  # event: the last result copy of buffer set p
+        for i in range(n):
+            p = i % 2
+            if computed[p] is not None:
+                s_in.wait_event(computed[p])
+            with torch.cuda.stream(s_in):
+                xalls[p].copy_(hx, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            if copied_out[p] is not None:
+                stream.wait_event(copied_out[p])
+            step(i, stream, p)
+            computed[p] = torch.cuda.Event()
+            computed[p].record(stream)
+            s_out.wait_event(computed[p])
+            with torch.cuda.stream(s_out):
+                hys[p].copy_(yalls[p], non_blocking=True)
+            copied_out[p] = torch.cuda.Event()
+            copied_out[p].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
     # The steps are recorded in a CUDA graph, as a decode loop would run them: every replayed
     # step still copies its inputs in and its results out (memcpy nodes), without the host's
     # per-call launch cost.  If the copies cannot be captured the steps run eagerly.
     e2e_spg = largest_divisor_le(e2e_steps, 20)
     with torch.cuda.stream(stream):
-        for i in range(5):
-            e2e_step(i)
+        e2e_steps_run(5)
     stream.synchronize()
     ge = None
     try:
         ge = torch.cuda.CUDAGraph()
         with torch.cuda.graph(ge, stream=stream):
-            for i in range(e2e_spg):
-                e2e_step(i)
+            e2e_steps_run(e2e_spg)
         with torch.cuda.stream(stream):
             ge.replay()
         stream.synchronize()
@@ -802,8 +839,7 @@ def run_ours(args, gemvs, rank, world):
             for _ in range(e2e_steps // e2e_spg):
                 ge.replay()
         else:
-            for i in range(e2e_steps):
-                e2e_step(i)
+            e2e_steps_run(e2e_steps)
         b.record(stream)
     stream.synchronize()
     e2e_ms = a.elapsed_time(b)
@@ -813,7 +849,9 @@ def run_ours(args, gemvs, rank, world):
            "ms_per_step": e2e_ms / e2e_steps,
            "how": ("CUDA graph of %d steps, replayed" % e2e_spg if ge is not None else "eager, stream-ordered")
                   + ": per step one pinned H2D copy of the step's packed x, one qgemv_run / qgemv_run_group / "
-                  "qgemv_run_batch per launch unit, one D2H copy of the packed outputs; weights resident"}
+                  "qgemv_run_batch per launch unit, one D2H copy of the packed outputs; weights resident; "
+                  "copies on two copy streams overlap the neighbouring steps' compute (two device buffer sets, "
+                  "event-ordered)"}
 
     configs = None
     if rank == 0 and not args.no_configs and B == 1:
