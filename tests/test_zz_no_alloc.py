@@ -7,8 +7,9 @@ within the GEMV tolerance of every parity test (|y - y_ref| <= 2e-3 * sum|x w| +
 and with qgemv_run's result within the same tolerance; two calls in a row give the same
 bits.  Covered: the shapes at
 the scratch limit exactly (N * ceil(K / 2048) equal to its capacity) and at the longest K
-(16 K-columns), and a call on a side stream.  The file is named to be collected last; it
-also passes on its own in a fresh process."""
+(16 K-columns), a call on a side stream, and a call captured in a CUDA graph on a side
+stream and replayed.  The file is named to be collected last; it also passes on its own in
+a fresh process."""
 import numpy as np
 import pytest
 import torch
@@ -87,6 +88,39 @@ def test_noalloc_at_the_scratch_limit_exactly(h):
 
 def test_noalloc_on_a_side_stream(h):
     _two_calls(h, synth.Q4_K, 1000, 14336, seed=8, stream=torch.cuda.Stream())
+
+
+def test_noalloc_in_a_cuda_graph_on_a_side_stream(h):
+    """Captured on a side stream after a warm-up call, then replayed twice with new activations
+    copied in between: each replay reads the x it finds and matches the oracle and qgemv_run on
+    that x."""
+    fmt, N, K = synth.Q4_K, 1000, 14336
+    W = synth.make_weights(fmt, N, K, 21)
+    Wd, _ = dev_bytes(W)
+    xs = [synth.make_x(fmt, K, 21 + i) for i in range(2)]
+    xd = dev_x(xs[0])
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    qgemv.run_noalloc(fmt, xd, Wd, N, K, y)  # the library's one-time set-up happens outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        qgemv.run_noalloc(fmt, xd, Wd, N, K, y, stream=side)
+    torch.cuda.synchronize()
+    for i, x in enumerate(xs):
+        xd.copy_(dev_x(x))
+        y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        y_ref, S = oracle.gemv(fmt, x, W, N, K)
+        yh = y.cpu().numpy()
+        assert_parity(yh, y_ref, S, f"noalloc graph replay {i}")
+        y_run = torch.empty(N, dtype=torch.float32, device="cuda")
+        qgemv.run(h, fmt, xd, Wd, N, K, y_run)
+        torch.cuda.synchronize()
+        assert_parity(yh, y_run.cpu().numpy().astype(np.float64), S, f"noalloc graph replay {i} against qgemv_run")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(h):
