@@ -817,7 +817,7 @@ def run_ours(args, gemvs, rank, world):
     # The steps are recorded in a CUDA graph, as a decode loop would run them: every replayed
     # step still copies its inputs in and its results out (memcpy nodes), without the host's
     # per-call launch cost.  If the copies cannot be captured the steps run eagerly.
-    e2e_spg = largest_divisor_le(e2e_steps, 20)
+    e2e_spg = largest_divisor_le(e2e_steps, 100)
     with torch.cuda.stream(stream):
         e2e_steps_run(5)
     stream.synchronize()
