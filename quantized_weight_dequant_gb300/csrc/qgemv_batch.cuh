@@ -1,8 +1,8 @@
 // Small-batch dequant GEMV: Y[m, n] = sum_k X[m, k] * dequant(W)[n, k] for M = 1..8
 // activation vectors, every weight decoded once and used by all of them.
 //
-// At M = 1 the product is a matrix-vector product and the streaming kernel's integer dot
-// products fit it best ("fp4_gemv" page: no MMA at M = 1); from a few vectors on, the same
+// At M = 1 the product is a matrix-vector product and the streaming kernel's exact
+// mixed-precision FMAs fit it best ("fp4_gemv" page: no MMA at M = 1); from a few vectors on, the same
 // decoded weight meets several activations, which is what the tensor cores' mma.sync
 // contraction does without any shared-memory round trip for the weights: they are decoded
 // in registers straight into the A fragments of m16n8k16 (16 weight rows as its M), and the

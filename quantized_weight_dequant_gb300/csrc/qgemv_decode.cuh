@@ -94,19 +94,6 @@ struct XStage {
 __device__ __forceinline__ int xq_slot(int i) { return i + (i >> 3); }
 __device__ __forceinline__ const uint16_t* xq_at(const uint16_t* q, int k) { return q + k + 8 * (k >> 6); }
 
-// d = c + a.h0 * b.b0 + a.h1 * b.b1 (lo) / a.h0 * b.b2 + a.h1 * b.b3 (hi); a two int16,
-// b four unsigned bytes.
-__device__ __forceinline__ int dp2a_lo_u(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp2a_hi_u(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 // max of the two unsigned 16-bit halves, lane-wise (sm_90+)
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;
